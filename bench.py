@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Throughput of the shared-memory-operand GEMM on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one GEMM C = A * B of the workload (default: M = N = K = 8192, bf16
+operands, A K-major, B N-major, fp32 accumulation, bf16 output), operands
+resident in HBM.  W untimed warm-up steps, then exactly K timed steps between a
+barrier + device synchronisation on both sides, CUDA events on the launching
+stream, max over ranks.  Operands + output (384 MiB) are larger than L2, so no
+flush is done between steps.  ``value`` = 2*M*N*K*steps*ranks / time.
+
+Multi-GPU (torchrun, N > 1): replicas only -- every rank runs its own full
+problem (weak scaling); the output tiles are independent, so no collective is
+on the data path.  ``--impl reference`` times the fp64 CPU oracle on the host
+cores instead (rank 0 only), on a bounded row slice of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "gemm_8192_bf16_bf16_AK_BN"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_NAME = "smo_gemm_kernel"
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shared_memory_operand_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"^kernel_source_hash:\s*(\S+)", text, re.M)
+    val = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+    if not src or not val or src.group(1) != kernel_source_hash():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks (identity on one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(flops_per_step: float, steps: int, world: int, max_seconds: float) -> dict:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    total = flops_per_step * steps * world
+    return {"value": total / max_seconds / 1e12, "ms_per_step": max_seconds * 1e3 / steps}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def oracle_rows_rate(p, target_s: float, max_rows: int = None):
+    """Times the fp64 oracle on the first r rows of the workload (full N, K),
+    r calibrated so the run takes about target_s.  Returns (TFLOP/s, rows,
+    seconds, threads)."""
+    from oracle import gemm as og
+    import torch
+
+    def run(rows):
+        if p.a_major == 0:
+            a_bits = p.A[: rows * p.lda].view(torch.int16).numpy().view("uint16")
+        else:
+            raise NotImplementedError("row slices need a K-major A")
+        b_bits = p.bits("B")
+        t0 = time.perf_counter()
+        og.gemm_f64(a_bits, p.lda, p.a_major, b_bits, p.ldb, p.b_major, p.in_dtype, rows, p.N,
+                    p.K, 1, 0, 0)
+        return time.perf_counter() - t0
+
+    t_small = run(4)
+    rows = max(4, min(max_rows or p.M, int(4 * target_s / max(t_small, 1e-3))))
+    dt = run(rows)
+    return 2.0 * rows * p.N * p.K / dt / 1e12, rows, dt, og.num_threads()
+
+
+# ------------------------------------------------------------------ arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from synthetic import workload
+    from oracle import gemm as og
+
+    p = workload(args.workload)
+    og.lib()
+    budget = min(4.0, 150.0 / max(1, args.steps + args.warmup))
+    # calibrate once, then each step computes the same bounded row slice
+    _, rows, dt, threads = oracle_rows_rate(p, budget)
+    import torch
+    a_bits = p.A[: rows * p.lda].view(torch.int16).numpy().view("uint16")
+    b_bits = p.bits("B")
+
+    def step():
+        og.gemm_f64(a_bits, p.lda, p.a_major, b_bits, p.ldb, p.b_major, p.in_dtype, rows, p.N, p.K,
+                    1, 0, 0)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * p.N * p.K
+    value = flops * args.steps / dt / 1e12
+    sample = f"first {rows} of {p.M} rows of the {args.workload} product (full N={p.N}, K={p.K}) per step"
+    line = {
+        "impl": "reference", "metric": "BF16 GEMM TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "M": p.M, "N": p.N, "K": p.K,
+                   "a_major": "K", "b_major": "N" if p.b_major else "K",
+                   "in": p.in_dtype, "out": p.out_dtype, "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import shared_memory_operand_gb300 as smo
+    from synthetic import workload
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    smo.load_library(build=True)
+    p = workload(args.workload)
+    dev = torch.device("cuda", local)
+    A = p.A.to(dev)
+    B = p.B.to(dev)
+    odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[p.out_dtype]
+    C = torch.empty(p.c_numel(), dtype=odt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch(a=A, b=B, c=C):
+        smo.gemm_ex(a, p.lda, p.a_major, b, p.ldb, p.b_major, c, p.ldc, p.M, p.N, p.K,
+                    in_dtype=p.in_dtype, out_dtype=p.out_dtype, batch=p.batch, strideA=p.strideA,
+                    strideB=p.strideB, strideC=p.strideC, stream=stream)
+
+    # one untimed launch, then the device error word must be clear
+    launch()
+    st = smo.gemm_check(stream)
+    if st != smo.GEMM_OK:
+        raise RuntimeError(smo.gemm_status_string(st))
+
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        launch()
+        ev[i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    total_s = t_start.elapsed_time(t_end) / 1e3
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    st = smo.gemm_check(stream)
+    if st != smo.GEMM_OK:
+        raise RuntimeError(smo.gemm_status_string(st))
+    max_s = reduce_max(total_s, world)
+    agg = aggregate(p.flops, args.steps, world, max_s)
+
+    # end to end: pinned host operands -> device, GEMM, C -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        Ah = p.A.pin_memory()
+        Bh = p.B.pin_memory()
+        Ch = torch.empty(C.numel(), dtype=odt).pin_memory()
+        e_steps = max(3, min(args.steps, 20))
+        for _ in range(2):
+            A.copy_(Ah, non_blocking=True)
+            B.copy_(Bh, non_blocking=True)
+            launch()
+            Ch.copy_(C, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(e_steps):
+            A.copy_(Ah, non_blocking=True)
+            B.copy_(Bh, non_blocking=True)
+            launch()
+            Ch.copy_(C, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e_s = reduce_max(e0.elapsed_time(e1) / 1e3, world)
+        e2e = {"value": p.flops * e_steps * world / e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(Ah.numel() * Ah.element_size() + Bh.numel() * Bh.element_size()),
+               "d2h_bytes_per_step": int(Ch.numel() * Ch.element_size()),
+               "steps": e_steps, "ms_per_step": e_s * 1e3 / e_steps}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = p.flops / avg_launch_s / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    alg_bytes = (p.M * p.K + p.K * p.N) * 2 * p.batch + p.M * p.N * C.element_size() * p.batch
+    traffic = profiled_traffic(args.workload)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "frac_of_sustained": achieved / peak_sus, "algorithmic_bytes": alg_bytes,
+                "kernel": KERNEL_NAME, "launch_ms_median": statistics.median(launch_ms)}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            rate, rows, dt, threads = oracle_rows_rate(p, args.cpu_seconds)
+            cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"first {rows} of {p.M} rows (full N, K) of the same product, "
+                             f"{dt:.1f} s"}
+        except NotImplementedError as e:
+            cpu = {"value": None, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": str(e)}
+
+    line = {
+        "metric": "BF16 GEMM TFLOP/s", "value": agg["value"], "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "M": p.M, "N": p.N, "K": p.K, "batch": p.batch,
+                   "a_major": "M" if p.a_major else "K", "b_major": "N" if p.b_major else "K",
+                   "in": p.in_dtype, "accumulate": "f32", "out": p.out_dtype,
+                   "dist": p.dist, "seed": p.seed, "parallelism": f"replicas{world}",
+                   "l2": "no flush: A+B+C resident set larger than L2 (129 MB)",
+                   "pct_of_dense_bf16_peak": 100.0 * agg["value"] / world / peak},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,134 @@
+/*
+ * smo_gemm.h -- C ABI of the shared-memory-operand GEMM library (libsmo_gemm.so)
+ *
+ * One operation: the dense matrix product C = A * B with 16-bit operands
+ * (bfloat16 or float16), fp32 accumulation in tensor memory, and fp32 / bf16 /
+ * f16 output.  Source of the operation: "An Educational GEMM Ladder for Helios
+ * GPUs", section "Educational GEMM Ladder" (every rung computes C = AB with
+ * A in R^{MxK}, B in R^{KxN}, BF16 inputs); the f16 variant is the GEMM of
+ * rocMLIR pull 2196's description (-m 1500 -n 1152 -k 896, f16).  Operands are
+ * staged through shared memory in 128-byte-swizzled layouts, and an
+ * N-contiguous ("transposed") B is consumed directly -- the role that
+ * "A Deep Dive into LDS Optimizations on AMD Instinct MI450 GPUs", Part I
+ * ("Why Is It Important?") gives to the transposed shared-memory load.
+ *
+ * Conventions shared by every entry point
+ *   Logical shapes: A is M x K, B is K x N, C is M x N (per batch entry).
+ *   Orientation ("major" = the contiguous dimension):
+ *     A, GEMM_K_MAJOR : A[m][k] at A[m*lda + k]      (row-major M x K)
+ *     A, GEMM_MN_MAJOR: A[m][k] at A[k*lda + m]      (M contiguous)
+ *     B, GEMM_K_MAJOR : B[k][n] at B[n*ldb + k]      (K contiguous per column)
+ *     B, GEMM_MN_MAJOR: B[k][n] at B[k*ldb + n]      (row-major K x N, N contiguous)
+ *     C               : C[m][n] at C[m*ldc + n]      (always row-major)
+ *   Batch entry b adds b*strideA / b*strideB / b*strideC elements.
+ *   Leading dimensions and strides are in elements.
+ *   Pointers: caller-owned DEVICE memory of the current CUDA device.  The
+ *   library keeps no reference after the call returns (the kernel reads and
+ *   writes them asynchronously on `stream`; keep them alive until it is done).
+ *   C is fully overwritten (alpha = 1, beta = 0).  C must not alias A or B.
+ *   Alignment (tensor-memory-accelerator rule): A, B, C 16-byte aligned; lda,
+ *   ldb and (batch > 1) strideA, strideB times the element size multiples of
+ *   16 bytes; the same for ldc and strideC with the output element size.
+ *   Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  No
+ *   entry point except gemm_check synchronises.
+ *   Allocation: the library allocates one 4-byte error word per device on its
+ *   first launch there and nothing per call.
+ *   Errors: every entry point returns GEMM_OK (0) or a negative gemm_status_t;
+ *   argument errors launch nothing and leave C untouched.
+ */
+#ifndef SMO_GEMM_H
+#define SMO_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
+typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_ARG = -1,          /* null pointer, negative size, ld below the row length, bad enum */
+    GEMM_ERR_ALIGN = -2,        /* base address / ld / stride breaks the 16-byte rules above */
+    GEMM_ERR_UNSUPPORTED = -3,  /* dtype combination, or a size beyond the library's limits */
+    GEMM_ERR_LAUNCH = -4,       /* the CUDA launch (or tensor-map encoding) failed */
+    GEMM_ERR_TIMEOUT = -5,      /* a bounded wait inside a kernel ran out (reported by gemm_check) */
+    GEMM_ERR_CUDA = -6,         /* another CUDA runtime error (see gemm_check) */
+    GEMM_ERR_NO_DEVICE = -7     /* no usable sm_103 device / driver entry point */
+} gemm_status_t;
+
+/*
+ * gemm_bf16: bf16 A and B, fp32 C, one problem.
+ * Equivalent to gemm_ex(..., GEMM_BF16, GEMM_F32, 1, 0, 0, 0, stream).
+ * a_major, b_major: gemm_major_t.  M, N, K >= 0; M == 0 or N == 0 is a no-op;
+ * K == 0 writes C = 0.
+ */
+int gemm_bf16(const void* A, int64_t lda, int a_major,
+              const void* B, int64_t ldb, int b_major,
+              void* C, int64_t ldc,
+              int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * gemm_ex: general entry point.
+ * in_dtype : GEMM_BF16 or GEMM_F16 (A and B share it).
+ * out_dtype: GEMM_F32, GEMM_BF16 or GEMM_F16 (fp32 accumulator rounded to
+ *            nearest-even on output).
+ * batch >= 1 independent problems; strideA/B/C are ignored when batch == 1.
+ */
+int gemm_ex(const void* A, int64_t lda, int a_major,
+            const void* B, int64_t ldb, int b_major,
+            void* C, int64_t ldc,
+            int64_t M, int64_t N, int64_t K,
+            int in_dtype, int out_dtype,
+            int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+            void* stream);
+
+/*
+ * gemm_check: synchronises `stream`, then reports the first error since the
+ * previous gemm_check on this device: GEMM_ERR_TIMEOUT if a kernel's bounded
+ * wait ran out (the kernel then returned early and C is incomplete),
+ * GEMM_ERR_CUDA for a CUDA error, else GEMM_OK.  Clears the device error word.
+ */
+int gemm_check(void* stream);
+
+/* Human-readable name of a gemm_status_t value (static string, never NULL). */
+const char* gemm_status_string(int status);
+
+/*
+ * gemm_set_timeout_ns: budget of every bounded wait inside the kernels, in
+ * nanoseconds of the GPU's global timer (default 2e9).  Values <= 0 restore the
+ * default.  Applies to launches made after the call.  Returns the old value.
+ */
+int64_t gemm_set_timeout_ns(int64_t ns);
+
+/*
+ * gemm_plan_describe: host-only.  Writes into buf (NUL-terminated, at most
+ * buflen bytes) a JSON description of the plan gemm_ex would use for these
+ * arguments on a GPU with num_sms multiprocessors: tile shape, pipeline depth,
+ * tensor-map boxes, tcgen05 instruction and shared-memory descriptors, the
+ * planner's F2 matrices of every shared-memory layout, its own layout checks
+ * and the shared-memory addresses the epilogue stores issue.  No GPU needed.
+ * Returns the length the full text needs (excluding the NUL), or a negative
+ * gemm_status_t if the arguments are invalid.
+ */
+int64_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, int a_major, int b_major,
+                           int in_dtype, int out_dtype, int64_t batch, int num_sms,
+                           char* buf, size_t buflen);
+
+/*
+ * gemm_debug_inject_stall: test hook.  When on != 0, the next launches skip the
+ * producer's first tensor-memory-accelerator load, so the consumer's bounded
+ * wait on that stage can never complete: the kernel times out (after the
+ * gemm_set_timeout_ns budget), sets GEMM_ERR_TIMEOUT and returns cleanly.
+ * Returns the previous setting.
+ */
+int gemm_debug_inject_stall(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMO_GEMM_H */

@@ -1,0 +1,285 @@
+// C ABI of the shared-memory-operand GEMM (declared in include/smo_gemm.h):
+// argument validation, plan cache, tensor-map encoding and the kernel launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "gemm_kernel.cuh"
+#include "planner.h"
+#include "smo_gemm.h"
+
+namespace {
+
+using smo::KParams;
+using smo::Plan;
+
+std::atomic<int64_t> g_timeout_ns{2000000000ll};
+std::atomic<int> g_stall{0};
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+    bool init = false;
+    bool usable = false;
+    int num_sms = 0;
+    int32_t* d_err = nullptr;
+    bool attr_set[3] = {false, false, false};
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+using PlanKey = std::tuple<int64_t, int64_t, int64_t, int, int, int, int, int64_t, int, int>;
+std::map<PlanKey, Plan> g_plans;
+
+int elem_size(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+
+CUtensorMapDataType tmap_type(int dt) {
+    return dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+         : dt == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+int force_bn_from_env() {
+    const char* s = std::getenv("SMO_GEMM_FORCE_BN");
+    if (!s) return 0;
+    int v = std::atoi(s);
+    return (v == 128 || v == 256) ? v : 0;
+}
+
+// Lazily initialises the per-device state of the current device.
+int device_state(DevState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState& d = g_dev[dev];
+    if (!d.init) {
+        d.init = true;
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        d.num_sms = sms;
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                    cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        if (major == 10 && minor == 3 && g_encode && cudaMalloc(&d.d_err, sizeof(int32_t)) == cudaSuccess &&
+            cudaMemset(d.d_err, 0, sizeof(int32_t)) == cudaSuccess) {
+            d.usable = true;
+        }
+        cudaGetLastError();
+    }
+    if (!d.usable) return GEMM_ERR_NO_DEVICE;
+    *out = &d;
+    return GEMM_OK;
+}
+
+// Argument checks shared by gemm_ex and gemm_plan_describe.
+int validate(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype, int out_dtype,
+             int64_t batch) {
+    if (M < 0 || N < 0 || K < 0 || batch < 1) return GEMM_ERR_ARG;
+    if ((a_major != GEMM_K_MAJOR && a_major != GEMM_MN_MAJOR) ||
+        (b_major != GEMM_K_MAJOR && b_major != GEMM_MN_MAJOR))
+        return GEMM_ERR_ARG;
+    if (in_dtype != GEMM_BF16 && in_dtype != GEMM_F16) return GEMM_ERR_UNSUPPORTED;
+    if (out_dtype != GEMM_BF16 && out_dtype != GEMM_F16 && out_dtype != GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) || batch >= (1ll << 31))
+        return GEMM_ERR_UNSUPPORTED;
+    return GEMM_OK;
+}
+
+const Plan* cached_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype, int out_dtype,
+                        int64_t batch, int num_sms) {
+    int fbn = force_bn_from_env();
+    PlanKey key{M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn};
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) return &it->second;
+    if (g_plans.size() > 4096) g_plans.clear();
+    Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn);
+    return &(g_plans[key] = p);
+}
+
+// 3-D tiled tensor map: dims {inner, outer, batch}, 128-byte swizzle.
+int encode(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint64_t batch, uint64_t ld,
+           uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+    const uint64_t es = (uint64_t)elem_size(dt);
+    cuuint64_t dims[3] = {inner, outer, batch};
+    uint64_t bstride = stride * es;
+    if (batch <= 1) {
+        bstride = ((ld * es * outer + 15) / 16) * 16;   // unused extent-1 dimension
+    }
+    cuuint64_t strides[2] = {ld * es, bstride};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, tmap_type(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
+}
+
+template <int OUT>
+int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+           const KParams& kp, cudaStream_t stream) {
+    auto kern = smo::smo_gemm_kernel<OUT>;
+    if (!ds.attr_set[OUT]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        ds.attr_set[OUT] = true;
+    }
+    kern<<<pl.grid, smo::kThreads, pl.smem_bytes, stream>>>(ta, tb, tc, kp);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C, int64_t ldc,
+            int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int64_t batch, int64_t strideA,
+            int64_t strideB, int64_t strideC, void* stream_) {
+    int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int64_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+    if (ldc < N) return GEMM_ERR_ARG;
+    if (batch > 1 && strideC < (M - 1) * ldc + N) return GEMM_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc * oes) % 16 || (batch > 1 && (strideC * oes) % 16))
+        return GEMM_ERR_ALIGN;
+    DevState* ds = nullptr;
+    if (K == 0) {
+        st = device_state(&ds);
+        if (st != GEMM_OK) return st;
+        for (int64_t b = 0; b < batch; ++b) {
+            char* cb = static_cast<char*>(C) + b * (batch > 1 ? strideC : 0) * oes;
+            if (cudaMemset2DAsync(cb, (size_t)(ldc * oes), 0, (size_t)(N * oes), (size_t)M, stream) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+        }
+        return GEMM_OK;
+    }
+    if (!A || !B) return GEMM_ERR_ARG;
+    const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
+    const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
+    if (lda < a_row || ldb < b_row) return GEMM_ERR_ARG;
+    if (batch > 1 && (strideA < 1 || strideB < 1)) return GEMM_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda * ies) % 16 ||
+        (ldb * ies) % 16 || (batch > 1 && ((strideA * ies) % 16 || (strideB * ies) % 16)))
+        return GEMM_ERR_ALIGN;
+
+    st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, ds->num_sms);
+    if (!pl->ok) return GEMM_ERR_UNSUPPORTED;
+
+    CUtensorMap ta, tb, tc;
+    const int64_t a_outer = (a_major == GEMM_MN_MAJOR) ? K : M;
+    const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
+    if (encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer) ||
+        encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer) ||
+        encode(&tc, out_dtype, C, N, M, batch, ldc, strideC, (uint32_t)pl->c.chunk_cols,
+               (uint32_t)smo::kEpiRowsPerWarp))
+        return GEMM_ERR_UNSUPPORTED;
+
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    smo::fill_params(*pl, &kp);
+    kp.err = ds->d_err;
+    kp.timeout_ns = g_timeout_ns.load();
+    kp.stall = g_stall.load();
+
+    switch (out_dtype) {
+        case GEMM_F32: return launch<smo::OUT_F32>(*pl, *ds, ta, tb, tc, kp, stream);
+        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, *ds, ta, tb, tc, kp, stream);
+        default: return launch<smo::OUT_F16>(*pl, *ds, ta, tb, tc, kp, stream);
+    }
+}
+
+int gemm_bf16(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C,
+              int64_t ldc, int64_t M, int64_t N, int64_t K, void* stream) {
+    return gemm_ex(A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, GEMM_BF16, GEMM_F32, 1, 0, 0, 0, stream);
+}
+
+int gemm_check(void* stream_) {
+    DevState* ds = nullptr;
+    int st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int32_t h = 0;
+    if (cudaMemcpy(&h, ds->d_err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (h != 0) {
+        cudaMemset(ds->d_err, 0, sizeof(int32_t));
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+const char* gemm_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_ARG: return "GEMM_ERR_ARG: invalid argument";
+        case GEMM_ERR_ALIGN: return "GEMM_ERR_ALIGN: pointer, leading dimension or stride not 16-byte aligned";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: unsupported dtype or size";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a bounded wait inside the kernel ran out";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime error";
+        case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no usable sm_103 device";
+        default: return "unknown status";
+    }
+}
+
+int64_t gemm_set_timeout_ns(int64_t ns) {
+    if (ns <= 0) ns = 2000000000ll;
+    return g_timeout_ns.exchange(ns);
+}
+
+int gemm_debug_inject_stall(int on) { return g_stall.exchange(on ? 1 : 0); }
+
+int64_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
+                           int out_dtype, int64_t batch, int num_sms, char* buf, size_t buflen) {
+    int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
+    if (st != GEMM_OK) return st;
+    Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms > 0 ? num_sms : 1,
+                            force_bn_from_env());
+    std::string s = smo::describe_json(p);
+    if (buf && buflen > 0) {
+        size_t n = s.size() < buflen - 1 ? s.size() : buflen - 1;
+        std::memcpy(buf, s.data(), n);
+        buf[n] = '\0';
+    }
+    return (int64_t)s.size();
+}
+
+}  // extern "C"

@@ -1,0 +1,279 @@
+// Persistent, warp-specialised BF16/F16 GEMM for sm_103a (GB300).
+//
+//   warp 0 (one thread)  TMA producer: fills a ring of `stages` shared-memory
+//                        stages with 128-byte-swizzled A and B tiles
+//                        (cp.async.bulk.tensor, mbarrier complete_tx).
+//   warp 1 (one thread)  MMA issuer: 4 x tcgen05.mma (128 x BN x 16) per stage,
+//                        accumulating in tensor memory; tcgen05.commit frees
+//                        the stage (split barrier) and, after the last K block,
+//                        publishes the accumulator.
+//   warps 2..5           epilogue: tcgen05.ld -> fp32/bf16/f16 -> conflict-free
+//                        swizzled st.shared -> TMA store (clips ragged edges).
+// Two tensor-memory accumulators let the epilogue of tile i overlap the main
+// loop of tile i + 1.
+//
+// Design lineage (prior art, re-made for tcgen05/TMA): "An Educational GEMM
+// Ladder for Helios GPUs" -- Level 1 (multi-buffered operand stages), Level 2
+// (direct global-to-shared copies), Level 3/4 (large output tiles, arithmetic
+// intensity 2MNK/(MK+KN+MN)), Level 5 (deep K per stage), Level 7 (descriptor
+// DMA issued by a single producer, zero fill at the K tail), Level 8 (split
+// barrier: release a stage as soon as its last MMA retires), Level 10
+// (epilogue staged through shared memory for wide coalesced stores), Level 12
+// (overlap of epilogue and main loop).  Operand orientation: an N-contiguous B
+// (or M-contiguous A) is consumed directly through the MN-major canonical
+// layout and the instruction descriptor's major bit -- the job the transposed
+// shared-memory load does in "A Deep Dive into LDS Optimizations on AMD
+// Instinct MI450 GPUs", Part I.
+//
+// Every mbarrier wait is bounded by p.timeout_ns of the global timer; on
+// timeout the thread records an error code, stops, and the CTA still drains
+// its in-flight copies and MMAs and frees tensor memory before returning.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace smo {
+
+__device__ __forceinline__ void report_error(int32_t* err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Tile id -> (batch, m block, n block), grouped along M for L2 reuse.
+__device__ __forceinline__ void decode_tile(const KParams& p, int64_t t, int& b, int& mb, int& nb) {
+    b = (int)(t / p.tiles_per_batch);
+    const int64_t r = t - (int64_t)b * p.tiles_per_batch;
+    const int64_t span = (int64_t)p.group_m * p.num_n;
+    const int g = (int)(r / span);
+    const int first_m = g * p.group_m;
+    const int gsz = min(p.num_m - first_m, p.group_m);
+    const int rr = (int)(r - (int64_t)g * span);
+    mb = first_m + rr % gsz;
+    nb = rr / gsz;
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
+    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
+    if (OUT == OUT_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);   // .x (low half) = a
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+template <int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    smo_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bars = base + p.off_bar;
+    auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bars + 8u * (kMaxStages + s); };
+    auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * kMaxStages + b); };
+    auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * kMaxStages + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * kMaxStages + 4);
+    const uint32_t tmem_slot = bars + 8u * (2 * kMaxStages + 5);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    const int64_t budget = p.timeout_ns;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per stage
+            bool skip_one = p.stall != 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+                int b, mb, nb;
+                decode_tile(p, t, b, mb, nb);
+                const int32_t m0 = mb * kBM, n0 = nb * p.BN;
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, budget)) {
+                        report_error(p.err, DEV_TIMEOUT_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    if (skip_one) {
+                        skip_one = false;          // test hook: this stage never fills
+                    } else {
+                        const uint32_t st = base + s * p.stage_stride;
+                        const int32_t k0 = kb * kBK;
+                        mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
+                        for (uint32_t j = 0; j < p.a_nbox; ++j) {
+                            const uint32_t dst = st + j * p.a_box_bytes;
+                            if (p.a_mn_major) tma_load_3d(dst, &tmA, full_bar(s), m0 + 64 * j, k0, b);
+                            else tma_load_3d(dst, &tmA, full_bar(s), k0, m0 + p.a_box_mn * j, b);
+                        }
+                        for (uint32_t j = 0; j < p.b_nbox; ++j) {
+                            const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
+                            if (p.b_mn_major) tma_load_3d(dst, &tmB, full_bar(s), n0 + 64 * j, k0, b);
+                            else tma_load_3d(dst, &tmB, full_bar(s), k0, n0 + p.b_box_mn * j, b);
+                        }
+                        issued_mask |= 1u << s;
+                        issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    }
+                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                }
+            }
+            // Every load this thread issued has landed before the CTA may exit
+            // (immediate when the consumer already waited for it).
+            for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
+                if ((issued_mask >> q) & 1u) {
+                    if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
+                        report_error(p.err, DEV_TIMEOUT_TEARDOWN);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
+                const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+                if (!mbar_wait(acce_bar(buf), aph ^ 1u, budget)) {
+                    report_error(p.err, DEV_TIMEOUT_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!mbar_wait(full_bar(s), ph, budget)) {
+                        report_error(p.err, DEV_TIMEOUT_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = base + s * p.stage_stride;
+                    const uint32_t b_addr = a_addr + p.b_off;
+                    const uint64_t a_desc = p.a_desc_hi | (uint64_t)((a_addr >> 4) & 0x3FFFu);
+                    const uint64_t b_desc = p.b_desc_hi | (uint64_t)((b_addr >> 4) & 0x3FFFu);
+#pragma unroll
+                    for (int k = 0; k < kBK / kMmaK; ++k) {
+                        umma_f16(d_tmem, a_desc + (uint64_t)((k * p.a_kstep) >> 4),
+                                 b_desc + (uint64_t)((k * p.b_kstep) >> 4), p.idesc, (kb | k) != 0);
+                    }
+                    umma_commit(empty_bar(s));     // stage free once these MMAs retire
+                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(accf_bar(buf));        // accumulator ready for the epilogue
+            }
+            // All MMAs issued by this thread have completed before teardown.
+            umma_commit(drain_bar);
+            if (!mbar_wait(drain_bar, 0, budget)) report_error(p.err, DEV_TIMEOUT_TEARDOWN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue
+        const uint32_t q = (uint32_t)warp & 3u;           // TMEM lane quarter of this warp
+        const uint32_t lane_field = (q * 32u) << 16;
+        uint32_t it = 0, sbuf = 0;
+        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+            int b, mb, nb;
+            decode_tile(p, t, b, mb, nb);
+            const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+            int good = 1;
+            if (lane == 0) good = mbar_wait(accf_bar(buf), aph, budget) ? 1 : 0;
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                if (lane == 0) report_error(p.err, DEV_TIMEOUT_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int32_t m0 = mb * kBM + (int32_t)q * kEpiRowsPerWarp;
+            for (int c = 0; c < p.epi_chunks; ++c) {
+                const uint32_t slab = base + p.off_epi + (q * kEpiBufs + sbuf) * kEpiSlabBytes;
+                if (lane == 0) bulk_wait_read<1>();        // this slab's previous store has read it
+                __syncwarp();
+                const uint32_t col = buf * (uint32_t)p.BN + (uint32_t)(c * p.epi_chunk_cols);
+                uint32_t v[32];
+                if (OUT == OUT_F32) {
+                    tmem_ld_32x32b_x32(tmem_base + lane_field + col, v);
+                    tmem_ld_wait();
+                } else {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_field + col, r0);
+                    tmem_ld_32x32b_x32(tmem_base + lane_field + col + 32, r1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        v[i] = pack2<OUT>(r0[2 * i], r0[2 * i + 1]);
+                        v[16 + i] = pack2<OUT>(r1[2 * i], r1[2 * i + 1]);
+                    }
+                }
+                if (c == p.epi_chunks - 1) {
+                    // accumulator fully read: hand it back to the MMA issuer
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(buf));
+                }
+                // Row `lane` of the slab; 16-byte chunk j goes to j ^ (row % 8):
+                // the 8 lanes of each store phase hit 8 different bank groups.
+                const uint32_t row = slab + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    st_shared_v4(row + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                 v[4 * j + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int32_t n0 = nb * p.BN + c * p.epi_chunk_cols;
+                    if (m0 < p.M && n0 < p.N) tma_store_3d(&tmC, slab, n0, m0, b);
+                    bulk_commit();
+                }
+                sbuf ^= 1u;
+            }
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+}
+
+}  // namespace smo

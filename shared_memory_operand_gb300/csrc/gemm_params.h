@@ -1,0 +1,57 @@
+// Kernel parameter block shared by the host planner and the sm_103a kernel.
+// Plain C++ (no CUDA headers) so the planner compiles with the host compiler.
+#pragma once
+#include <stdint.h>
+
+namespace smo {
+
+constexpr int kBM = 128;            // output rows per tile (tcgen05 M, cta_group::1)
+constexpr int kBK = 64;             // K per pipeline stage: 64 x 16-bit = one 128-byte swizzle row
+constexpr int kMmaK = 16;           // K per tcgen05.mma.kind::f16
+constexpr int kThreads = 192;       // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kEpiRowsPerWarp = 32;
+constexpr int kEpiBufs = 2;         // staging buffers per epilogue warp
+constexpr uint32_t kEpiSlabBytes = kEpiRowsPerWarp * 128;   // 32 rows x 128 B
+constexpr int kMaxStages = 8;
+constexpr uint32_t kSmemLimit = 232448;                      // 227 KiB opt-in per block
+constexpr uint32_t kBarrierBytes = 256;
+
+// Out element types.
+enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
+
+// Error codes written to the device error word (first writer wins).
+enum DevErr : int32_t {
+    DEV_OK = 0,
+    DEV_TIMEOUT_PRODUCER = 1,
+    DEV_TIMEOUT_MMA = 2,
+    DEV_TIMEOUT_EPILOGUE = 3,
+    DEV_TIMEOUT_TEARDOWN = 4,
+};
+
+struct KParams {
+    int32_t M, N, K, batch;
+    int32_t num_m, num_n, num_k;
+    int32_t group_m;
+    int64_t tiles_per_batch, total_tiles;
+    int32_t BN, stages;
+    uint32_t idesc;                 // tcgen05 instruction descriptor
+    uint32_t a_mn_major, b_mn_major;
+    uint32_t a_nbox, b_nbox;        // TMA boxes per stage and operand
+    uint32_t a_box_bytes, b_box_bytes;
+    uint32_t a_box_mn, b_box_mn;    // MN extent of one box
+    uint32_t a_kstep, b_kstep;      // descriptor start-address advance per 16-wide K step (bytes)
+    uint64_t a_desc_hi, b_desc_hi;  // smem descriptor fields other than the start address
+    uint32_t stage_stride;          // bytes per pipeline stage (A then B)
+    uint32_t b_off;                 // offset of B inside a stage
+    uint32_t off_epi, off_bar;      // from the 1024-aligned smem base
+    uint32_t tmem_cols;
+    uint32_t tx_bytes;              // bytes TMA delivers per stage
+    int32_t epi_chunk_cols;         // output columns per 128-byte chunk
+    int32_t epi_chunks;             // chunks per tile row (BN / epi_chunk_cols)
+    int32_t* err;                   // device error word
+    int64_t timeout_ns;             // budget of each bounded wait
+    int32_t stall;                  // test hook: skip the first TMA load
+};
+
+}  // namespace smo

@@ -1,0 +1,319 @@
+// Layout planner (host C++): see planner.h.
+#include "planner.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <set>
+#include <sstream>
+#include <vector>
+
+namespace smo {
+namespace {
+
+constexpr uint32_t kSwizzleSpan = 128;        // bytes per swizzled row
+constexpr uint32_t kSwizzleAtom = 1024;       // 8 rows x 128 B
+
+// 128-byte swizzle of a byte offset inside a 1024-byte aligned region: the
+// 16-byte chunk index (bits 4..6) is XORed with the row-in-atom (bits 7..9).
+inline uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+
+int log2i(uint32_t v) {
+    int r = 0;
+    while ((1u << r) < v) ++r;
+    return r;
+}
+
+// Where TMA (SWIZZLE_128B, box inner extent 128 bytes) puts element (mn, k) of
+// a stage tile.
+uint32_t tma_offset(const OperandPlan& op, uint32_t mn, uint32_t k) {
+    if (!op.mn_major) {
+        // one box: outer = mn rows of 128 bytes (64 k values)
+        return sw128(mn * kSwizzleSpan + k * 2);
+    }
+    // boxes of 64 mn x 64 k: box j = mn / 64, row = k, byte = 2 * (mn % 64)
+    uint32_t j = mn / 64;
+    return j * op.box_bytes + sw128(k * kSwizzleSpan + (mn % 64) * 2);
+}
+
+// Where the tensor core reads element (mn, k) given the descriptor fields
+// (canonical SWIZZLE_128B layouts of the tcgen05 shared-memory descriptor),
+// the start address advanced by kstep per 16-wide K step.
+uint32_t umma_offset(const OperandPlan& op, uint32_t mn, uint32_t k) {
+    uint32_t step = k / kMmaK, kk = k % kMmaK;
+    uint32_t start = step * op.kstep;
+    uint32_t pre;
+    if (!op.mn_major) {
+        // ((8,m),(T,2)) : ((8T,SBO),(1,T)), T = 16 bytes
+        pre = start + (mn % 8) * 128 + (mn / 8) * op.sbo + kk * 2;
+    } else {
+        // ((T,8,m),(8,2)) : ((1,T,LBO),(8T,SBO))
+        pre = start + (mn % 64) * 2 + (mn / 64) * op.lbo + (kk % 8) * 128 + (kk / 8) * op.sbo;
+    }
+    return sw128(pre);
+}
+
+uint64_t desc_hi(uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;     // leading dimension byte offset
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;     // stride dimension byte offset
+    d |= (uint64_t)1 << 46;                          // fixed 0b001 (tcgen05 descriptor version)
+    d |= (uint64_t)2 << 61;                          // layout: SWIZZLE_128B
+    return d;                                        // base offset 0 (1024-aligned stages)
+}
+
+void plan_operand(OperandPlan& op, int mn_major, int tile_mn) {
+    op.mn_major = mn_major;
+    op.tile_mn = tile_mn;
+    if (!mn_major) {
+        op.box_inner = kBK;              // K, 128 bytes
+        op.box_outer = tile_mn;          // MN rows
+        op.nbox = 1;
+        op.box_bytes = tile_mn * kSwizzleSpan;
+        op.lbo = 16;                     // unused by swizzled K-major layouts
+        op.sbo = kSwizzleAtom;           // next group of 8 rows
+        op.kstep = kMmaK * 2;            // 32 bytes along the swizzled row
+    } else {
+        op.box_inner = 64;               // MN, 128 bytes
+        op.box_outer = kBK;              // K rows
+        op.nbox = tile_mn / 64;
+        op.box_bytes = kBK * kSwizzleSpan;
+        op.lbo = op.box_bytes;           // next 64-wide MN atom = next box
+        op.sbo = kSwizzleAtom;           // next group of 8 k rows
+        op.kstep = 2 * kSwizzleAtom;     // 16 k rows
+    }
+    op.stage_bytes = op.box_bytes * op.nbox;
+    op.desc_hi = desc_hi(op.lbo, op.sbo);
+
+    // ---- F2 model and checks ------------------------------------------------
+    op.bits_mn = log2i(tile_mn);
+    op.bits_k = log2i(kBK);
+    for (int i = 0; i < op.bits_mn; ++i) op.basis_mn[i] = tma_offset(op, 1u << i, 0);
+    for (int i = 0; i < op.bits_k; ++i) op.basis_k[i] = tma_offset(op, 0, 1u << i);
+    bool linear = true, same = true;
+    std::vector<uint8_t> hit(op.stage_bytes / 2, 0);
+    bool inj = true;
+    for (uint32_t mn = 0; mn < (uint32_t)tile_mn; ++mn) {
+        for (uint32_t k = 0; k < (uint32_t)kBK; ++k) {
+            uint32_t t = tma_offset(op, mn, k);
+            uint32_t x = 0;
+            for (int i = 0; i < op.bits_mn; ++i) if ((mn >> i) & 1) x ^= op.basis_mn[i];
+            for (int i = 0; i < op.bits_k; ++i) if ((k >> i) & 1) x ^= op.basis_k[i];
+            linear &= (x == t);
+            same &= (umma_offset(op, mn, k) == t);
+            if (t / 2 >= hit.size() || hit[t / 2]) inj = false; else hit[t / 2] = 1;
+        }
+    }
+    op.linear = linear;
+    op.tma_equals_umma = same;
+    op.bijective = inj && std::all_of(hit.begin(), hit.end(), [](uint8_t h) { return h != 0; });
+    // Left division by the 16-byte contiguous row of a core matrix: the first
+    // three bases of the contiguous dimension must be 2, 4, 8 bytes and every
+    // other basis a multiple of 16 bytes.
+    const uint32_t* cont = op.mn_major ? op.basis_mn : op.basis_k;
+    int ncont = op.mn_major ? op.bits_mn : op.bits_k;
+    bool div = ncont >= 3 && cont[0] == 2 && cont[1] == 4 && cont[2] == 8;
+    for (int i = 3; i < ncont; ++i) div &= (cont[i] % 16) == 0;
+    const uint32_t* other = op.mn_major ? op.basis_k : op.basis_mn;
+    int nother = op.mn_major ? op.bits_k : op.bits_mn;
+    for (int i = 0; i < nother; ++i) div &= (other[i] % 16) == 0;
+    op.core_matrix_divides = div;
+}
+
+// Epilogue staging: warp-private slabs of 32 rows x 128 bytes, 128-byte
+// swizzled; lane l stores 16-byte chunk j of row l.
+uint32_t epi_offset(uint32_t row, uint32_t chunk) { return sw128(row * 128 + chunk * 16); }
+
+int bank_degree_16B(const uint32_t* addr, int lanes) {
+    // 32 banks x 4 bytes; 16-byte accesses served 8 lanes per phase.
+    int worst = 0;
+    for (int p = 0; p < lanes; p += 8) {
+        std::set<uint32_t> words[32];
+        for (int l = p; l < p + 8 && l < lanes; ++l)
+            for (uint32_t w = addr[l] / 4; w < (addr[l] + 16) / 4; ++w) words[w % 32].insert(w);
+        for (auto& s : words) worst = std::max<int>(worst, (int)s.size());
+    }
+    return worst;
+}
+
+}  // namespace
+
+uint32_t make_idesc(int in_dtype, int a_mn_major, int b_mn_major, int M, int N) {
+    uint32_t fmt = (in_dtype == 0) ? 1u : 0u;     // BF16 = 1, F16 = 0
+    uint32_t d = 0;
+    d |= 1u << 4;                                  // D format: F32
+    d |= fmt << 7;                                 // A format
+    d |= fmt << 10;                                // B format
+    d |= (uint32_t)(a_mn_major & 1) << 15;         // A major: 0 K, 1 MN
+    d |= (uint32_t)(b_mn_major & 1) << 16;         // B major
+    d |= (uint32_t)((N >> 3) & 0x3F) << 17;        // N >> 3
+    d |= (uint32_t)((M >> 4) & 0x1F) << 24;        // M >> 4
+    return d;
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
+               int out_dtype, int64_t batch, int num_sms, int force_bn) {
+    Plan p;
+    p.M = M; p.N = N; p.K = K; p.batch = batch;
+    p.in_dtype = in_dtype; p.out_dtype = out_dtype;
+    p.num_sms = num_sms > 0 ? num_sms : 1;
+    if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) || batch >= (1ll << 31)) {
+        p.why = "dimension beyond 2^31-1";
+        return p;
+    }
+    p.num_m = (int)((M + kBM - 1) / kBM);
+    p.num_k = (int)((K + kBK - 1) / kBK);
+    auto tiles_for = [&](int bn) { return (int64_t)p.num_m * ((N + bn - 1) / bn) * batch; };
+    int bn = 256;
+    if (force_bn == 128 || force_bn == 256) {
+        bn = force_bn;
+    } else {
+        // Wave quantisation: a 128-wide tile costs a bit over half a 256-wide one.
+        int64_t t256 = tiles_for(256), t128 = tiles_for(128);
+        double c256 = (double)((t256 + p.num_sms - 1) / p.num_sms) * 1.0;
+        double c128 = (double)((t128 + p.num_sms - 1) / p.num_sms) * 0.55;
+        bn = (c128 < c256) ? 128 : 256;
+    }
+    p.BN = bn;
+    p.num_n = (int)((N + bn - 1) / bn);
+    p.tiles = tiles_for(bn);
+    p.grid = (int)std::min<int64_t>(p.tiles, p.num_sms);
+    p.group_m = std::min(16, p.num_m);
+    p.idesc = make_idesc(in_dtype, a_major, b_major, kBM, bn);
+
+    plan_operand(p.a, a_major, kBM);
+    plan_operand(p.b, b_major, bn);
+
+    p.c.out_es = (out_dtype == 2) ? 4 : 2;
+    p.c.chunk_cols = 128 / p.c.out_es;
+    p.c.chunks = bn / p.c.chunk_cols;
+    for (int i = 0; i < 5; ++i) p.c.basis_row[i] = epi_offset(1u << i, 0);
+    for (int i = 0; i < 3; ++i) p.c.basis_chunk[i] = epi_offset(0, 1u << i);
+    {
+        std::set<uint32_t> offs;
+        bool lin = true;
+        for (uint32_t r = 0; r < 32; ++r)
+            for (uint32_t c = 0; c < 8; ++c) {
+                uint32_t o = epi_offset(r, c);
+                uint32_t x = 0;
+                for (int i = 0; i < 5; ++i) if ((r >> i) & 1) x ^= p.c.basis_row[i];
+                for (int i = 0; i < 3; ++i) if ((c >> i) & 1) x ^= p.c.basis_chunk[i];
+                lin &= (x == o);
+                offs.insert(o);
+            }
+        p.c.bijective = lin && offs.size() == 256 && *offs.rbegin() == kEpiSlabBytes - 16;
+        int worst = 0;
+        for (uint32_t j = 0; j < 8; ++j) {
+            uint32_t addr[32];
+            for (uint32_t l = 0; l < 32; ++l) addr[l] = epi_offset(l, j);
+            worst = std::max(worst, bank_degree_16B(addr, 32));
+        }
+        p.c.planner_degree = worst;
+    }
+
+    // Shared-memory carve-up (offsets from a 1024-byte aligned base).
+    p.stage_stride = p.a.stage_bytes + p.b.stage_bytes;
+    uint32_t epi_bytes = kEpiWarps * kEpiBufs * kEpiSlabBytes;
+    uint32_t fixed = 1024 /* alignment slack */ + epi_bytes + kBarrierBytes;
+    int stages = (int)((kSmemLimit - fixed) / p.stage_stride);
+    stages = std::min(stages, kMaxStages);
+    if (stages < 2) {
+        p.why = "shared memory too small for two stages";
+        return p;
+    }
+    p.stages = stages;
+    p.off_epi = stages * p.stage_stride;
+    p.off_bar = p.off_epi + epi_bytes;
+    p.smem_bytes = p.off_bar + kBarrierBytes + 1024;
+    p.tmem_cols = 2 * bn;                          // two accumulators (power of two >= 32)
+
+    bool layouts_ok = p.a.linear && p.a.bijective && p.a.tma_equals_umma && p.a.core_matrix_divides &&
+                      p.b.linear && p.b.bijective && p.b.tma_equals_umma && p.b.core_matrix_divides &&
+                      p.c.bijective && p.c.planner_degree == 1;
+    if (!layouts_ok) {
+        p.why = "layout check failed";
+        return p;
+    }
+    p.ok = true;
+    return p;
+}
+
+void fill_params(const Plan& p, KParams* kp) {
+    kp->M = (int32_t)p.M; kp->N = (int32_t)p.N; kp->K = (int32_t)p.K; kp->batch = (int32_t)p.batch;
+    kp->num_m = p.num_m; kp->num_n = p.num_n; kp->num_k = p.num_k;
+    kp->group_m = p.group_m;
+    kp->tiles_per_batch = (int64_t)p.num_m * p.num_n;
+    kp->total_tiles = p.tiles;
+    kp->BN = p.BN; kp->stages = p.stages;
+    kp->idesc = p.idesc;
+    kp->a_mn_major = p.a.mn_major; kp->b_mn_major = p.b.mn_major;
+    kp->a_nbox = p.a.nbox; kp->b_nbox = p.b.nbox;
+    kp->a_box_bytes = p.a.box_bytes; kp->b_box_bytes = p.b.box_bytes;
+    kp->a_box_mn = p.a.mn_major ? 64 : p.a.box_outer;
+    kp->b_box_mn = p.b.mn_major ? 64 : p.b.box_outer;
+    kp->a_kstep = p.a.kstep; kp->b_kstep = p.b.kstep;
+    kp->a_desc_hi = p.a.desc_hi; kp->b_desc_hi = p.b.desc_hi;
+    kp->stage_stride = p.stage_stride;
+    kp->b_off = p.a.stage_bytes;
+    kp->off_epi = p.off_epi; kp->off_bar = p.off_bar;
+    kp->tmem_cols = p.tmem_cols;
+    kp->tx_bytes = p.stage_stride;
+    kp->epi_chunk_cols = p.c.chunk_cols;
+    kp->epi_chunks = p.c.chunks;
+}
+
+std::string describe_json(const Plan& p) {
+    std::ostringstream o;
+    auto op_json = [&](const OperandPlan& a) {
+        o << "{\"mn_major\":" << a.mn_major << ",\"tile_mn\":" << a.tile_mn
+          << ",\"box\":[" << a.box_inner << "," << a.box_outer << "],\"nbox\":" << a.nbox
+          << ",\"box_bytes\":" << a.box_bytes << ",\"stage_bytes\":" << a.stage_bytes
+          << ",\"lbo\":" << a.lbo << ",\"sbo\":" << a.sbo << ",\"kstep_bytes\":" << a.kstep
+          << ",\"desc_hi\":" << a.desc_hi << ",\"swizzle\":\"128B\"";
+        o << ",\"basis_mn\":[";
+        for (int i = 0; i < a.bits_mn; ++i) o << (i ? "," : "") << a.basis_mn[i];
+        o << "],\"basis_k\":[";
+        for (int i = 0; i < a.bits_k; ++i) o << (i ? "," : "") << a.basis_k[i];
+        o << "],\"linear\":" << (a.linear ? "true" : "false")
+          << ",\"bijective\":" << (a.bijective ? "true" : "false")
+          << ",\"tma_equals_umma\":" << (a.tma_equals_umma ? "true" : "false")
+          << ",\"core_matrix_divides\":" << (a.core_matrix_divides ? "true" : "false") << "}";
+    };
+    o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
+      << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
+      << ",\"BM\":" << kBM << ",\"BN\":" << p.BN << ",\"BK\":" << kBK << ",\"mma_k\":" << kMmaK
+      << ",\"stages\":" << p.stages << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
+      << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
+      << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads
+      << ",\"idesc\":" << p.idesc << ",\"smem_bytes\":" << p.smem_bytes
+      << ",\"stage_stride\":" << p.stage_stride << ",\"off_epi\":" << p.off_epi
+      << ",\"off_bar\":" << p.off_bar << ",\"tmem_cols\":" << p.tmem_cols;
+    o << ",\"A\":";
+    op_json(p.a);
+    o << ",\"B\":";
+    op_json(p.b);
+    o << ",\"C\":{\"out_es\":" << p.c.out_es << ",\"chunk_cols\":" << p.c.chunk_cols
+      << ",\"chunks\":" << p.c.chunks << ",\"slab_bytes\":" << kEpiSlabBytes
+      << ",\"bufs\":" << kEpiBufs << ",\"basis_row\":[";
+    for (int i = 0; i < 5; ++i) o << (i ? "," : "") << p.c.basis_row[i];
+    o << "],\"basis_chunk\":[";
+    for (int i = 0; i < 3; ++i) o << (i ? "," : "") << p.c.basis_chunk[i];
+    o << "],\"bijective\":" << (p.c.bijective ? "true" : "false")
+      << ",\"planner_degree\":" << p.c.planner_degree;
+    // Addresses (from the aligned smem base) of the 8 st.shared.v4 of one chunk
+    // for every epilogue warp slot and staging buffer.
+    o << ",\"store_addrs\":[";
+    bool first = true;
+    for (uint32_t w = 0; w < (uint32_t)kEpiWarps; ++w)
+        for (uint32_t sb = 0; sb < (uint32_t)kEpiBufs; ++sb)
+            for (uint32_t j = 0; j < 8; ++j) {
+                o << (first ? "" : ",") << "[";
+                first = false;
+                uint32_t base = p.off_epi + (w * kEpiBufs + sb) * kEpiSlabBytes;
+                for (uint32_t l = 0; l < 32; ++l) o << (l ? "," : "") << base + epi_offset(l, j);
+                o << "]";
+            }
+    o << "]}}";
+    return o.str();
+}
+
+}  // namespace smo

@@ -1,0 +1,73 @@
+// Layout planner: chooses the tile, the pipeline depth, the TMA boxes and the
+// tcgen05 descriptors, and proves on the host -- by modelling every
+// shared-memory layout as an F2-linear map from element coordinates to byte
+// offsets -- that the layout TMA writes is the layout the tensor core reads.
+//
+// Linear-layout view: "A Deep Dive into LDS Optimizations on AMD Instinct MI450
+// GPUs", "A Linear Layout Refresher" (a layout is a binary matrix on index
+// bits; images XOR) and "Dividing Layouts" (left division = block-diagonal
+// factor; here the factor is the 16-byte contiguous core-matrix row).
+// XOR swizzle: "LDS Optimization" skill page, "Optimization Method 1: Swizzle
+// Layout" (col ^= f(row)); mask width rule from "Choosing Swizzle Parameters"
+// (32 banks, 16-byte vectors -> a 3-bit mask, i.e. the 128-byte swizzle).
+#pragma once
+#include <stdint.h>
+#include <string>
+
+#include "gemm_params.h"
+
+namespace smo {
+
+struct OperandPlan {
+    int mn_major = 0;
+    int tile_mn = 0;                // rows of the operand tile in its MN dimension
+    uint32_t box_inner = 0, box_outer = 0;   // TMA box (elements)
+    int nbox = 0;
+    uint32_t box_bytes = 0, stage_bytes = 0;
+    uint32_t lbo = 0, sbo = 0, kstep = 0;
+    uint64_t desc_hi = 0;
+    // F2 model of the stage tile: byte offset of unit coordinates
+    int bits_mn = 0, bits_k = 0;
+    uint32_t basis_mn[16] = {0}, basis_k[16] = {0};
+    bool linear = false, bijective = false, tma_equals_umma = false, core_matrix_divides = false;
+};
+
+struct EpiPlan {
+    int out_es = 4;
+    int chunk_cols = 32;
+    int chunks = 0;
+    uint32_t basis_row[5] = {0}, basis_chunk[3] = {0};
+    bool bijective = false;
+    int planner_degree = 0;         // planner's own bank-degree estimate of one store
+};
+
+struct Plan {
+    int64_t M = 0, N = 0, K = 0, batch = 1;
+    int in_dtype = 0, out_dtype = 0;
+    int BN = 256, stages = 4;
+    int num_m = 0, num_n = 0, num_k = 0, group_m = 16;
+    int64_t tiles = 0;
+    int grid = 0, num_sms = 0;
+    uint32_t idesc = 0;
+    OperandPlan a, b;
+    EpiPlan c;
+    uint32_t stage_stride = 0, off_epi = 0, off_bar = 0, smem_bytes = 0, tmem_cols = 0;
+    bool ok = false;
+    std::string why;                // reason when !ok
+};
+
+// in_dtype: 0 bf16, 1 f16.  out_dtype: 0 bf16, 1 f16, 2 f32 (gemm_dtype_t).
+// force_bn: 0 = choose, else 128 or 256.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
+               int out_dtype, int64_t batch, int num_sms, int force_bn);
+
+// Fills the kernel parameter block from a plan (pointers and runtime knobs are
+// set by the caller).
+void fill_params(const Plan& p, KParams* kp);
+
+std::string describe_json(const Plan& p);
+
+// tcgen05 instruction descriptor for kind::f16 with fp32 accumulation.
+uint32_t make_idesc(int in_dtype, int a_mn_major, int b_mn_major, int M, int N);
+
+}  // namespace smo

@@ -1,0 +1,163 @@
+"""Host-side checks of the C-ABI library (no GPU): it builds, loads and exports
+every symbol the header declares; arguments are validated before any device
+work; and the layout planner's F2 model of every shared-memory layout agrees
+with the oracle's independent restatement and bank simulator."""
+import os
+import re
+
+import pytest
+
+import shared_memory_operand_gb300 as smo
+from oracle import banksim
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return smo.load_library(build=True)
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "smo_gemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"if", "defined"})
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _header_functions()
+    assert set(names) == set(smo.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for st in range(0, -8, -1):
+        s = smo.gemm_status_string(st)
+        assert s and s != "unknown status"
+    assert smo.gemm_status_string(-99) == "unknown status"
+
+
+def _ex(A=0x1000, lda=64, am=0, B=0x2000, ldb=64, bm=1, C=0x3000, ldc=64, M=64, N=64, K=64,
+        i=0, o=2, batch=1, sa=0, sb=0, sc=0):
+    return smo.gemm_ex_status(A, lda, am, B, ldb, bm, C, ldc, M, N, K, i, o, batch, sa, sb, sc,
+                              stream=0)
+
+
+def test_argument_validation_without_device(lib):
+    assert _ex(am=2) == smo.GEMM_ERR_ARG
+    assert _ex(bm=-1) == smo.GEMM_ERR_ARG
+    assert _ex(M=-1) == smo.GEMM_ERR_ARG
+    assert _ex(batch=0) == smo.GEMM_ERR_ARG
+    assert _ex(i=2) == smo.GEMM_ERR_UNSUPPORTED        # f32 operands
+    assert _ex(o=7) == smo.GEMM_ERR_UNSUPPORTED
+    assert _ex(M=0) == smo.GEMM_OK                       # empty product: no-op
+    assert _ex(N=0, C=0) == smo.GEMM_OK
+    assert _ex(C=0) == smo.GEMM_ERR_ARG
+    assert _ex(A=0) == smo.GEMM_ERR_ARG
+    assert _ex(ldc=63) == smo.GEMM_ERR_ARG
+    assert _ex(lda=63) == smo.GEMM_ERR_ARG
+    assert _ex(am=1, lda=64, M=65) == smo.GEMM_ERR_ARG  # M-major A needs lda >= M
+    assert _ex(A=0x1008) == smo.GEMM_ERR_ALIGN
+    assert _ex(C=0x3004) == smo.GEMM_ERR_ALIGN
+    assert _ex(lda=68, K=66) == smo.GEMM_ERR_ALIGN      # 136-byte pitch
+    assert _ex(o=0, ldc=68, N=66) == smo.GEMM_ERR_ALIGN
+    assert _ex(batch=2, sa=64 * 64, sb=64 * 64, sc=64) == smo.GEMM_ERR_ARG   # C batches overlap
+    assert _ex(batch=2, sa=4100, sb=4096, sc=4096) == smo.GEMM_ERR_ALIGN
+    assert _ex(M=1 << 31) == smo.GEMM_ERR_UNSUPPORTED
+    # well-formed arguments reach the device query: no GPU here
+    if not _have_gpu():
+        assert _ex() == smo.GEMM_ERR_NO_DEVICE
+        assert smo.gemm_check(0) == smo.GEMM_ERR_NO_DEVICE
+
+
+def _have_gpu():
+    import torch
+    return torch.cuda.is_available()
+
+
+def test_timeout_knob(lib):
+    old = smo.gemm_set_timeout_ns(12345)
+    assert smo.gemm_set_timeout_ns(0) == 12345
+    assert smo.gemm_set_timeout_ns(old) == 2_000_000_000
+
+
+SHAPES = [(256, 256, 256), (1500, 1152, 896), (4096, 4096, 4096), (8192, 8192, 8192),
+          (16384, 8192, 1024), (1, 1, 1), (129, 257, 65)]
+
+
+@pytest.mark.parametrize("am", [0, 1])
+@pytest.mark.parametrize("bm", [0, 1])
+@pytest.mark.parametrize("out", ["f32", "bf16", "f16"])
+def test_planner_layouts_match_oracle(lib, am, bm, out):
+    for (M, N, K) in SHAPES:
+        d = smo.gemm_plan_describe(M, N, K, am, bm, "bf16", out)
+        assert d["ok"], d["why"]
+        assert d["smem_bytes"] <= 232448
+        assert d["tmem_cols"] == 2 * d["BN"] and d["tmem_cols"] <= 512
+        for name, major, tile in (("A", am, d["BM"]), ("B", bm, d["BN"])):
+            op = d[name]
+            mn_major = bool(major)
+            # planner's F2 basis images == oracle's 128B-swizzle TMA box layout
+            want_mn = [banksim.operand_tile_offset(1 << i, 0, mn_major, tile)
+                       for i in range(tile.bit_length() - 1)]
+            want_k = [banksim.operand_tile_offset(0, 1 << i, mn_major, tile) for i in range(6)]
+            assert op["basis_mn"] == want_mn
+            assert op["basis_k"] == want_k
+            # descriptor strides: the oracle's canonical layout with the
+            # planner's LBO / SBO / K step reproduces the TMA layout exactly
+            for mn in range(0, tile, 3):
+                for k in range(64):
+                    assert banksim.umma_canonical_offset(mn, k, mn_major, op["lbo"], op["sbo"],
+                                                         op["kstep_bytes"]) == \
+                        banksim.operand_tile_offset(mn, k, mn_major, tile)
+            assert op["linear"] and op["bijective"] and op["tma_equals_umma"]
+            assert op["core_matrix_divides"]
+            assert op["stage_bytes"] == tile * 64 * 2
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_epilogue_stores_conflict_free(lib, out):
+    d = smo.gemm_plan_describe(1024, 1024, 1024, 0, 1, "bf16", out)
+    c = d["C"]
+    assert c["chunk_cols"] * (4 if out == "f32" else 2) == 128
+    seen = set()
+    for addrs in c["store_addrs"]:
+        rep = banksim.simulate(addrs, 16)
+        assert rep.degree == 1, addrs
+        assert rep.wavefronts == 4
+        for a in addrs:
+            assert a % 16 == 0
+            assert d["off_epi"] <= a < d["off_bar"]
+            seen.update(range(a, a + 16))
+    # 4 warps x 2 buffers x 4 KiB, every byte written by exactly one (lane, store)
+    assert len(seen) == 4 * 2 * 4096
+    # the same chunk without the swizzle: the 8-way control
+    rows = [c["store_addrs"][0][0] + 128 * l for l in range(32)]
+    assert banksim.simulate(rows, 16).degree == 8
+
+
+def test_instruction_descriptor_fields(lib):
+    """Field layout of the tcgen05 kind::f16 instruction descriptor (PTX ISA):
+    D fmt bits 4-5, A fmt 7-9, B fmt 10-12, A/B major 15/16, N>>3 17-22,
+    M>>4 24-28."""
+    for am in (0, 1):
+        for bm in (0, 1):
+            for ind, fmt in (("bf16", 1), ("f16", 0)):
+                d = smo.gemm_plan_describe(2048, 2048, 2048, am, bm, ind, "f32")
+                x = d["idesc"]
+                assert (x >> 4) & 3 == 1
+                assert (x >> 7) & 7 == fmt and (x >> 10) & 7 == fmt
+                assert (x >> 15) & 1 == am and (x >> 16) & 1 == bm
+                assert ((x >> 17) & 63) * 8 == d["BN"]
+                assert ((x >> 24) & 31) * 16 == 128
+                assert x & 0b1111 == 0 and (x >> 13) & 3 == 0 and (x >> 23) & 1 == 0
+
+
+def test_tile_choice_and_grid(lib):
+    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
+    assert d["BN"] == 128 and d["tiles"] == 12 * 9 and d["grid"] == 108
+    d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
+    assert d["BN"] == 256 and d["tiles"] == 64 * 32 and d["grid"] == 152
+    d = smo.gemm_plan_describe(2048, 2048, 2048, 0, 1, "bf16", "bf16", batch=32)
+    assert d["tiles"] == 16 * 8 * 32

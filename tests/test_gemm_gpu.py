@@ -1,0 +1,178 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small and ragged shapes are compared element by element over the whole output;
+the full-size configurations are compared on sampled outputs (the oracle
+computes each one as its own dot product) in the launch configuration the bench
+times.  Integer-valued inputs must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import shared_memory_operand_gb300 as smo
+from synthetic import K_MAJOR, MN_MAJOR, make_problem, workload
+from tests.gemm_check import check, oracle_full, oracle_sampled, run_gpu, sample_positions
+
+pytestmark = pytest.mark.gpu
+
+MAJORS = [(K_MAJOR, K_MAJOR), (K_MAJOR, MN_MAJOR), (MN_MAJOR, K_MAJOR), (MN_MAJOR, MN_MAJOR)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    smo.load_library(build=True)
+    yield
+
+
+def _full(p, exact=False, stream=None):
+    gpu = run_gpu(p, stream=stream)
+    return check(p, gpu, oracle_full(p), exact=exact)
+
+
+# ------------------------------------------------------------ small / ragged
+@pytest.mark.parametrize("am,bm", MAJORS)
+@pytest.mark.parametrize("ind,out", [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f32"), ("f16", "f16")])
+def test_small_ragged_all_orientations(am, bm, ind, out):
+    for (M, N, K) in [(128, 256, 64), (300, 520, 200), (129, 257, 65), (1, 8, 1), (7, 9, 8)]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype=ind, out_dtype=out,
+                         dist="uniform", seed=M + N + K)
+        _full(p)
+
+
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_integer_inputs_bit_exact(am, bm):
+    for (M, N, K) in [(384, 640, 448), (131, 200, 1000)]:
+        for out in ("f32", "bf16"):
+            p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="bf16", out_dtype=out,
+                             dist="int", seed=3)
+            _full(p, exact=True)
+
+
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_permutation_operands_exact(am, bm):
+    """A wrong descriptor stride or major bit permutes K or N: a permutation
+    matrix operand exposes which rows or columns moved."""
+    g = torch.Generator().manual_seed(1)
+    K, N, M = 192, 256, 256
+    for trial in range(2):
+        p = make_problem(M, N, K, a_major=am, b_major=bm, dist="uniform", seed=trial)
+        perm = torch.randperm(K, generator=g)
+        P = torch.zeros(M, K)
+        P[torch.arange(M), perm[torch.arange(M) % K]] = 1.0
+        p.logical_A()[0].copy_(P.to(torch.bfloat16))
+        _full(p, exact=True)
+        # and B a column-permutation of the identity (K x N)
+        q = make_problem(M, N, K, a_major=am, b_major=bm, dist="uniform", seed=10 + trial)
+        Q = torch.zeros(K, N)
+        rows = torch.randperm(K, generator=g)
+        Q[rows[torch.arange(N) % K], torch.arange(N)] = 1.0
+        q.logical_B()[0].copy_(Q.to(torch.bfloat16))
+        _full(q, exact=True)
+
+
+def test_k_tails_and_padding():
+    for K in (1, 15, 16, 17, 63, 64, 65, 127, 1000):
+        p = make_problem(200, 300, K, a_major=K_MAJOR, b_major=MN_MAJOR, dist="uniform", seed=K,
+                         ld_extra=24)
+        _full(p)
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    p = make_problem(100, 72, 0, out_dtype="f32")
+    gpu = run_gpu(p)
+    assert np.all(gpu == 0.0)
+    C = torch.full((8, 8), 7.0, device="cuda")
+    smo.gemm_ex(0, 8, 0, 0, 8, 1, C, 8, 0, 8, 8, out_dtype="f32")
+    torch.cuda.synchronize()
+    assert torch.all(C == 7.0)
+
+
+def test_batched_small():
+    for am, bm in MAJORS:
+        p = make_problem(130, 200, 96, a_major=am, b_major=bm, batch=5, dist="normal",
+                         sigma=0.5, seed=2, out_dtype="bf16")
+        _full(p)
+
+
+def test_side_stream_and_repeat():
+    s = torch.cuda.Stream()
+    p = make_problem(512, 512, 512, dist="uniform", seed=8, out_dtype="f32")
+    ref = oracle_full(p)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            check(p, run_gpu(p, stream=s), ref)
+
+
+def test_gemm_bf16_entry_point():
+    p = make_problem(256, 256, 256, dist="uniform", out_dtype="f32")
+
+    def call(A, lda, am, B, ldb, bm, C, ldc, M, N, K, **kw):
+        smo.gemm_bf16(A, lda, am, B, ldb, bm, C, ldc, M, N, K, stream=kw.get("stream"))
+    check(p, run_gpu(p, fn=call), oracle_full(p))
+
+
+def test_bounded_wait_timeout_reports_and_recovers():
+    old = smo.gemm_set_timeout_ns(20_000_000)          # 20 ms
+    try:
+        smo.gemm_debug_inject_stall(True)
+        A = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
+        B = torch.zeros(256, 256, dtype=torch.bfloat16, device="cuda")
+        C = torch.zeros(256, 256, dtype=torch.float32, device="cuda")
+        smo.gemm_ex(A, 256, 0, B, 256, 1, C, 256, 256, 256, 256, out_dtype="f32")
+        assert smo.gemm_check() == smo.GEMM_ERR_TIMEOUT
+    finally:
+        smo.gemm_debug_inject_stall(False)
+        smo.gemm_set_timeout_ns(old)
+    assert smo.gemm_check() == smo.GEMM_OK              # error word cleared
+    p = make_problem(256, 256, 256, dist="uniform", out_dtype="f32")
+    check(p, run_gpu(p), oracle_full(p))                 # context still healthy
+
+
+# ------------------------------------------------------------ the configurations
+def test_config_256_bf16_f32():
+    _full(workload("gemm_256_bf16_f32"))
+
+
+def test_config_1500x1152x896_f16_uniform():
+    _full(workload("gemm_1500x1152x896_f16_f32"))
+
+
+def test_config_1500x1152x896_f16_integer_bit_exact():
+    _full(workload("gemm_1500x1152x896_f16_f32_int"), exact=True)
+
+
+def _sampled(p, count=3000):
+    gpu = run_gpu(p)
+    bi, mi, ni = sample_positions(p, count)
+    ref = oracle_sampled(p, bi, mi, ni)
+    check(p, gpu[bi, mi, ni], ref)
+    assert np.all(np.isfinite(gpu))
+    return gpu
+
+
+@pytest.mark.parametrize("name", ["gemm_4096_bf16_bf16_AK_BK", "gemm_4096_bf16_bf16_AK_BN",
+                                  "gemm_4096_bf16_bf16_AM_BK", "gemm_4096_bf16_bf16_AM_BN"])
+def test_config_4096_all_orientations(name):
+    _sampled(workload(name))
+
+
+@pytest.mark.parametrize("name", ["gemm_8192_bf16_bf16_AK_BN", "gemm_8192_bf16_bf16_AK_BK"])
+def test_config_8192(name):
+    _sampled(workload(name), count=2000)
+
+
+def test_config_8192_integer_bit_exact():
+    """Integers in [-4, 4]: |partial sums| <= 16 * 8192 < 2^24, exact in fp32."""
+    p = workload("gemm_8192_bf16_bf16_AK_BN", dist="int", out_dtype="f32")
+    gpu = run_gpu(p)
+    bi, mi, ni = sample_positions(p, 4000)
+    check(p, gpu[bi, mi, ni], oracle_sampled(p, bi, mi, ni), exact=True)
+
+
+def test_config_skinny():
+    _sampled(workload("skinny_16384x8192x1024_bf16"))
+
+
+def test_config_batched():
+    _sampled(workload("batched_32x2048_bf16"), count=4000)
