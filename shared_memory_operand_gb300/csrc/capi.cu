@@ -197,18 +197,25 @@ int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb,
     const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, ds->num_sms);
     if (!pl->ok) return GEMM_ERR_UNSUPPORTED;
 
+    // TMA stores write whole 16-byte pieces, so the C map covers only the
+    // 16-byte-aligned prefix of each row; the kernel stores the rest directly.
+    const int64_t n_tma = (N * oes / 16) * 16 / oes;
     CUtensorMap ta, tb, tc;
     const int64_t a_outer = (a_major == GEMM_MN_MAJOR) ? K : M;
     const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
     if (encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer) ||
         encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer) ||
-        encode(&tc, out_dtype, C, N, M, batch, ldc, strideC, (uint32_t)pl->c.chunk_cols,
-               (uint32_t)smo::kEpiRowsPerWarp))
+        encode(&tc, out_dtype, C, (uint64_t)(n_tma > 0 ? n_tma : 16 / oes), M, batch, ldc, strideC,
+               (uint32_t)pl->c.chunk_cols, (uint32_t)smo::kEpiRowsPerWarp))
         return GEMM_ERR_UNSUPPORTED;
 
     KParams kp;
     std::memset(&kp, 0, sizeof(kp));
     smo::fill_params(*pl, &kp);
+    kp.C = C;
+    kp.ldc = ldc;
+    kp.strideC = batch > 1 ? strideC : 0;
+    kp.n_tma = (int32_t)n_tma;
     kp.err = ds->d_err;
     kp.timeout_ns = g_timeout_ns.load();
     kp.stall = g_stall.load();

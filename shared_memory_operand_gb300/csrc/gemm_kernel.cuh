@@ -72,6 +72,8 @@ template <int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+    constexpr int kOutBytes = (OUT == OUT_F32) ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
@@ -258,10 +260,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
+                const int32_t n0 = nb * p.BN + c * p.epi_chunk_cols;
                 if (lane == 0) {
-                    const int32_t n0 = nb * p.BN + c * p.epi_chunk_cols;
-                    if (m0 < p.M && n0 < p.N) tma_store_3d(&tmC, slab, n0, m0, b);
+                    if (m0 < p.M && n0 < p.n_tma) tma_store_3d(&tmC, slab, n0, m0, b);
                     bulk_commit();
+                }
+                if (n0 + p.epi_chunk_cols > p.n_tma && n0 < p.N) {
+                    // TMA stores write whole 16-byte pieces at the row end; the
+                    // last < 16 bytes of a ragged row are stored from registers.
+                    const int32_t m = m0 + lane;
+                    if (m < p.M) {
+                        char* rowp = static_cast<char*>(p.C) +
+                                     ((int64_t)b * p.strideC + (int64_t)m * p.ldc) * kOutBytes;
+#pragma unroll
+                        for (int i = 0; i < kChunkCols; ++i) {
+                            const int32_t n = n0 + i;
+                            if (n >= p.n_tma && n < p.N) {
+                                if (OUT == OUT_F32)
+                                    *reinterpret_cast<uint32_t*>(rowp + (int64_t)n * 4) = v[i];
+                                else
+                                    *reinterpret_cast<uint16_t*>(rowp + (int64_t)n * 2) =
+                                        (uint16_t)(v[i >> 1] >> (16 * (i & 1)));
+                            }
+                        }
+                    }
                 }
                 sbuf ^= 1u;
             }

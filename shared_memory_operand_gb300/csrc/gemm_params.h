@@ -49,6 +49,9 @@ struct KParams {
     uint32_t tx_bytes;              // bytes TMA delivers per stage
     int32_t epi_chunk_cols;         // output columns per 128-byte chunk
     int32_t epi_chunks;             // chunks per tile row (BN / epi_chunk_cols)
+    void* C;                        // output base (ragged 16-byte row tails are stored directly)
+    int64_t ldc, strideC;           // elements
+    int32_t n_tma;                  // columns [0, n_tma) are written by TMA (n_tma * es % 16 == 0)
     int32_t* err;                   // device error word
     int64_t timeout_ns;             // budget of each bounded wait
     int32_t stall;                  // test hook: skip the first TMA load
