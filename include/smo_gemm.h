@@ -127,6 +127,41 @@ int64_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, int a_major, int b_m
  */
 int gemm_debug_inject_stall(int on);
 
+/*
+ * gemm_ex_noalloc: gemm_ex for callers that cannot allocate device memory.
+ * The paper has no counterpart of this entry point; it exists for users of
+ * this library, not for the method.
+ *
+ * Who needs it: callers whose device memory is owned entirely by a pool or
+ * arena allocator (framework caching allocators, inference runtimes that hand
+ * a plugin a fixed workspace and forbid other allocations), and callers that
+ * must not allocate once they are running (latency-critical serving loops,
+ * where cudaMalloc may synchronise the device).  gemm_ex allocates one 4-byte
+ * error word per device on its first launch there; this entry point allocates
+ * nothing: its kernel's scratch (the same error word) lives in a file-scope
+ * device array of 256 bytes (64 words, word 0 used), which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Arguments, layouts, ownership and return codes are those of gemm_ex.  Sizes:
+ * the scratch needed is one word for every problem size the library accepts;
+ * dimensions or batch >= 2^31 are rejected with GEMM_ERR_UNSUPPORTED.
+ * Set-up: the first call on a device (made with that device current) resolves
+ * the array's device address once (cudaGetSymbolAddress); make that first call
+ * before any stream capture.
+ * Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Every call shares the array: each call clears the error word on `stream`
+ * (cudaMemsetAsync) before its launch, so calls that overlap on the GPU race on
+ * it.  A bounded-wait timeout of this variant is recorded only in that shared
+ * word (gemm_check does not read it); C is then incomplete.
+ */
+int gemm_ex_noalloc(const void* A, int64_t lda, int a_major,
+                    const void* B, int64_t ldb, int b_major,
+                    void* C, int64_t ldc,
+                    int64_t M, int64_t N, int64_t K,
+                    int in_dtype, int out_dtype,
+                    int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32}
 
 # Every symbol include/smo_gemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_ex", "gemm_check", "gemm_status_string", "gemm_set_timeout_ns",
-           "gemm_plan_describe", "gemm_debug_inject_stall")
+           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc")
 
 
 class GemmError(RuntimeError):
@@ -55,6 +55,9 @@ def load_library(path: str = LIB_PATH, build: bool = False) -> ctypes.CDLL:
     L.gemm_ex.restype = i32
     L.gemm_ex.argtypes = [vp, i64, i32, vp, i64, i32, vp, i64, i64, i64, i64, i32, i32, i64, i64, i64,
                           i64, vp]
+    L.gemm_ex_noalloc.restype = i32
+    L.gemm_ex_noalloc.argtypes = [vp, i64, i32, vp, i64, i32, vp, i64, i64, i64, i64, i32, i32, i64,
+                                  i64, i64, i64, vp]
     L.gemm_check.restype = i32
     L.gemm_check.argtypes = [vp]
     L.gemm_status_string.restype = ctypes.c_char_p
@@ -118,6 +121,15 @@ def gemm_ex(A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype="bf16", 
                                 _dt(in_dtype), _dt(out_dtype), batch, strideA, strideB, strideC,
                                 _stream(stream))
     _raise(st, "gemm_ex")
+
+
+def gemm_ex_noalloc(A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype="bf16",
+                    out_dtype="f32", batch=1, strideA=0, strideB=0, strideC=0, stream=None) -> None:
+    """gemm_ex without any device allocation (scratch in a static device array)."""
+    st = load_library().gemm_ex_noalloc(_ptr(A), lda, a_major, _ptr(B), ldb, b_major, _ptr(C), ldc,
+                                        M, N, K, _dt(in_dtype), _dt(out_dtype), batch, strideA,
+                                        strideB, strideC, _stream(stream))
+    _raise(st, "gemm_ex_noalloc")
 
 
 def gemm_ex_status(*args, **kw) -> int:

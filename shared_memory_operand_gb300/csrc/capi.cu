@@ -152,6 +152,62 @@ int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMa
     return GEMM_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant (gemm_ex_noalloc).  The kernel's only scratch memory
+// is its 32-bit error word; here it lives in a file-scope device array instead
+// of a cudaMalloc'd word, so this path allocates no device memory at all.  The
+// array is part of the library's module: every GPU that loads the library
+// holds it (256 bytes) until the process exits.
+constexpr int kNoAllocScratchWords = 64;   // 256 bytes; the kernel uses word 0
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchWords];
+
+struct NoAllocState {
+    bool init = false;
+    bool usable = false;
+    DevState ds;                 // SM count and launch-attribute flags (ds.d_err unused)
+    int32_t* scratch = nullptr;  // device address of g_noalloc_scratch
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Once per device, with that device current: resolve the device address of the
+// static scratch array (host code may not use the symbol itself as a pointer).
+int noalloc_state(NoAllocState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    NoAllocState& n = g_noalloc[dev];
+    if (!n.init) {
+        n.init = true;
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        n.ds.num_sms = sms;
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                    cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        void* ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e == cudaSuccess && ptr != nullptr && major == 10 && minor == 3 && g_encode) {
+            n.scratch = static_cast<int32_t*>(ptr);
+            n.ds.usable = true;
+            n.usable = true;
+        }
+        cudaGetLastError();
+    }
+    if (!n.usable) return GEMM_ERR_NO_DEVICE;
+    *out = &n;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -287,6 +343,85 @@ int64_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, int a_major, int b_m
         buf[n] = '\0';
     }
     return (int64_t)s.size();
+}
+
+int gemm_ex_noalloc(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C,
+                    int64_t ldc, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int64_t batch,
+                    int64_t strideA, int64_t strideB, int64_t strideC, void* stream_) {
+    // Sizes: the scratch this variant needs is one word whatever the problem
+    // size; problems beyond the library's limits (any dimension or batch
+    // >= 2^31) are rejected here with GEMM_ERR_UNSUPPORTED.
+    int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return GEMM_ERR_ARG;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const int64_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+    if (ldc < N) return GEMM_ERR_ARG;
+    if (batch > 1 && strideC < (M - 1) * ldc + N) return GEMM_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc * oes) % 16 || (batch > 1 && (strideC * oes) % 16))
+        return GEMM_ERR_ALIGN;
+    NoAllocState* na = nullptr;
+    if (K == 0) {
+        st = noalloc_state(&na);
+        if (st != GEMM_OK) return st;
+        for (int64_t b = 0; b < batch; ++b) {
+            char* cb = static_cast<char*>(C) + b * (batch > 1 ? strideC : 0) * oes;
+            if (cudaMemset2DAsync(cb, (size_t)(ldc * oes), 0, (size_t)(N * oes), (size_t)M, stream) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+        }
+        return GEMM_OK;
+    }
+    if (!A || !B) return GEMM_ERR_ARG;
+    const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
+    const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
+    if (lda < a_row || ldb < b_row) return GEMM_ERR_ARG;
+    if (batch > 1 && (strideA < 1 || strideB < 1)) return GEMM_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda * ies) % 16 ||
+        (ldb * ies) % 16 || (batch > 1 && ((strideA * ies) % 16 || (strideB * ies) % 16)))
+        return GEMM_ERR_ALIGN;
+
+    st = noalloc_state(&na);
+    if (st != GEMM_OK) return st;
+    const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, na->ds.num_sms);
+    if (!pl->ok) return GEMM_ERR_UNSUPPORTED;
+
+    const int64_t n_tma = (N * oes / 16) * 16 / oes;
+    CUtensorMap ta, tb, tc;
+    const int64_t a_outer = (a_major == GEMM_MN_MAJOR) ? K : M;
+    const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
+    if (encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer) ||
+        encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer) ||
+        encode(&tc, out_dtype, C, (uint64_t)(n_tma > 0 ? n_tma : 16 / oes), M, batch, ldc, strideC,
+               (uint32_t)pl->c.chunk_cols, (uint32_t)smo::kEpiRowsPerWarp))
+        return GEMM_ERR_UNSUPPORTED;
+
+    // The shared array keeps the previous call's contents: the error word must
+    // start at zero for this launch (memset on the stream, no allocation).
+    if (cudaMemsetAsync(na->scratch, 0, sizeof(int32_t), stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    smo::fill_params(*pl, &kp);
+    kp.C = C;
+    kp.ldc = ldc;
+    kp.strideC = batch > 1 ? strideC : 0;
+    kp.n_tma = (int32_t)n_tma;
+    kp.err = na->scratch;
+    kp.timeout_ns = g_timeout_ns.load();
+    kp.stall = g_stall.load();
+
+    switch (out_dtype) {
+        case GEMM_F32: return launch<smo::OUT_F32>(*pl, na->ds, ta, tb, tc, kp, stream);
+        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, na->ds, ta, tb, tc, kp, stream);
+        default: return launch<smo::OUT_F16>(*pl, na->ds, ta, tb, tc, kp, stream);
+    }
 }
 
 }  // extern "C"
