@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
@@ -13,6 +14,7 @@
 #include <tuple>
 
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_pair.cuh"
 #include "planner.h"
 #include "smo_gemm.h"
 
@@ -32,6 +34,8 @@ struct DevState {
     int num_sms = 0;
     int32_t* d_err = nullptr;
     bool attr_set[3] = {false, false, false};
+    bool pair_attr_set[3] = {false, false, false};
+    int pair_max_clusters[3] = {0, 0, 0};   // co-resident 2-CTA clusters of the pair kernel
 };
 
 std::mutex g_mu;
@@ -53,7 +57,7 @@ int force_bn_from_env() {
     const char* s = std::getenv("SMO_GEMM_FORCE_BN");
     if (!s) return 0;
     int v = std::atoi(s);
-    return (v == 128 || v == 256) ? v : 0;
+    return (v == 128 || v == 256 || v == 512) ? v : 0;
 }
 
 // Lazily initialises the per-device state of the current device.
@@ -136,8 +140,8 @@ int encode(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t out
 }
 
 template <int OUT>
-int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-           const KParams& kp, cudaStream_t stream) {
+int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
+                  const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
     auto kern = smo::smo_gemm_kernel<OUT>;
     if (!ds.attr_set[OUT]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
@@ -150,6 +154,55 @@ int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMa
     kern<<<pl.grid, smo::kThreads, pl.smem_bytes, stream>>>(ta, tb, tc, kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
+}
+
+// CTA-pair kernel: clusters of two CTAs, one per SM; the persistent grid is
+// as many clusters as can be co-resident (at most one per tile).
+template <int OUT>
+int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
+                const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
+    auto kern = smo::smo_gemm_pair_kernel<OUT>;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(smo::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (!ds.pair_attr_set[OUT]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        cfg.gridDim = dim3(2 * (unsigned)std::max(1, ds.num_sms / 2), 1, 1);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        ds.pair_max_clusters[OUT] = n;
+        ds.pair_attr_set[OUT] = true;
+    }
+    const int64_t clusters = std::min<int64_t>(pl.tiles, ds.pair_max_clusters[OUT]);
+    cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+template <int OUT>
+int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+           const KParams& kp, cudaStream_t stream) {
+    return pl.pair ? launch_pair<OUT>(pl, ds, ta, tb, tc, kp, stream)
+                   : launch_single<OUT>(pl, ds, ta, tb, tc, kp, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,0 +1,121 @@
+// Device pieces shared by the one-CTA and CTA-pair GEMM kernels: error
+// reporting, tile decoding and the epilogue (tensor memory -> registers ->
+// 128-byte-swizzled shared-memory slab -> TMA store, ragged row tails stored
+// directly).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace smo {
+
+__device__ __forceinline__ void report_error(int32_t* err, int32_t code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Tile id -> (batch, m block, n block), grouped along M for L2 reuse.
+__device__ __forceinline__ void decode_tile(const KParams& p, int64_t t, int& b, int& mb, int& nb) {
+    b = (int)(t / p.tiles_per_batch);
+    const int64_t r = t - (int64_t)b * p.tiles_per_batch;
+    const int64_t span = (int64_t)p.group_m * p.num_n;
+    const int g = (int)(r / span);
+    const int first_m = g * p.group_m;
+    const int gsz = min(p.num_m - first_m, p.group_m);
+    const int rr = (int)(r - (int64_t)g * span);
+    mb = first_m + rr % gsz;
+    nb = rr / gsz;
+}
+
+template <int OUT>
+__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
+    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
+    if (OUT == OUT_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);   // .x (low half) = a
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Epilogue of one accumulator tile for one warp: its 32 rows (TMEM lanes
+// 32*(warp % 4) ...), all p.epi_chunks column chunks of 128 bytes.
+//   tmem_acc : tensor-memory address of the accumulator (lane field 0)
+//   slabs    : this warp's first staging slab (kEpiBufs slabs of kEpiSlabBytes)
+//   m0, n0   : first output row of the warp and first column of the tile
+// `release` is called once every accumulator column has been read, so the MMA
+// issuer may overwrite the accumulator while the stores drain.
+template <int OUT, typename Release>
+__device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
+                                              uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
+                                              int32_t m0, int32_t n0, int b, Release release) {
+    constexpr int kOutBytes = (OUT == OUT_F32) ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;
+    for (int c = 0; c < p.epi_chunks; ++c) {
+        const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
+        if (lane == 0) bulk_wait_read<1>();        // this slab's previous store has read it
+        __syncwarp();
+        const uint32_t col = (uint32_t)(c * kChunkCols);
+        uint32_t v[32];
+        if (OUT == OUT_F32) {
+            tmem_ld_32x32b_x32(tmem_acc + lane_field + col, v);
+            tmem_ld_wait();
+        } else {
+            uint32_t r0[32], r1[32];
+            tmem_ld_32x32b_x32(tmem_acc + lane_field + col, r0);
+            tmem_ld_32x32b_x32(tmem_acc + lane_field + col + 32, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                v[i] = pack2<OUT>(r0[2 * i], r0[2 * i + 1]);
+                v[16 + i] = pack2<OUT>(r1[2 * i], r1[2 * i + 1]);
+            }
+        }
+        if (c == p.epi_chunks - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+        // Row `lane` of the slab; 16-byte chunk j goes to j ^ (row % 8): the 8
+        // lanes of each store phase hit 8 different bank groups.
+        const uint32_t row = slab + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            st_shared_v4(row + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int32_t nc = n0 + c * kChunkCols;
+        if (lane == 0) {
+            if (m0 < p.M && nc < p.n_tma) tma_store_3d(tmC, slab, nc, m0, b);
+            bulk_commit();
+        }
+        if (nc + kChunkCols > p.n_tma && nc < p.N) {
+            // TMA stores write whole 16-byte pieces at the row end; the last
+            // < 16 bytes of a ragged row are stored from registers.
+            const int32_t m = m0 + lane;
+            if (m < p.M) {
+                char* rowp = static_cast<char*>(p.C) + ((int64_t)b * p.strideC + (int64_t)m * p.ldc) * kOutBytes;
+#pragma unroll
+                for (int i = 0; i < kChunkCols; ++i) {
+                    const int32_t n = nc + i;
+                    if (n >= p.n_tma && n < p.N) {
+                        if (OUT == OUT_F32)
+                            *reinterpret_cast<uint32_t*>(rowp + (int64_t)n * 4) = v[i];
+                        else
+                            *reinterpret_cast<uint16_t*>(rowp + (int64_t)n * 2) =
+                                (uint16_t)(v[i >> 1] >> (16 * (i & 1)));
+                    }
+                }
+            }
+        }
+        sbuf ^= 1u;
+    }
+}
+
+}  // namespace smo

@@ -1,0 +1,217 @@
+// CTA-pair variant of the persistent GEMM for sm_103a: 256 x 256 output tiles
+// computed by two CTAs of a cluster with tcgen05.mma.cta_group::2.
+//
+// Each CTA of the pair holds its own 128 rows of A and its own 128 columns of
+// B per pipeline stage (32 KiB per stage, 6 stages); the even CTA's single MMA
+// thread issues 256 x 256 x 16 MMAs that read both CTAs' shared memory and
+// accumulate rows 0..127 in the even CTA's tensor memory and rows 128..255 in
+// the odd CTA's.  Compared with one CTA per 128 x 256 tile this halves the
+// B bytes each SM stages per flop and doubles the pipeline depth for the same
+// shared memory ("An Educational GEMM Ladder for Helios GPUs", Level 4: larger
+// output tiles raise arithmetic intensity; Level 9: a cluster of workgroups
+// shares operand panels instead of re-requesting them).
+//
+// Synchronisation across the pair:
+//   full[s]    (even CTA only) -- both CTAs' TMA loads complete on it
+//                                 (cp.async.bulk.tensor ... .cta_group::2);
+//                                 the even producer arms it for both CTAs' bytes
+//   empty[s]   (both)          -- the MMA thread's commit multicasts to both
+//   acc_full   (both)          -- likewise, after the last K block of a tile
+//   acc_empty  (even CTA only) -- 4 epilogue warps of each CTA arrive
+// Every wait is bounded; cluster barriers at start (barriers initialised,
+// tensor memory allocated) and end (no CTA leaves while its peer may still
+// signal it).
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "gemm_common.cuh"
+
+namespace smo {
+
+template <int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    smo_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank() & 1u;      // 0: even CTA of the pair, issues the MMAs
+    const uint32_t lead = cluster_ctarank() & ~1u;     // cluster rank of the even CTA
+
+    const uint32_t bars = base + p.off_bar;
+    auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bars + 8u * (kMaxStages + s); };
+    auto accf_bar = [&](uint32_t b) { return bars + 8u * (2 * kMaxStages + b); };
+    auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * kMaxStages + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * kMaxStages + 4);
+    const uint32_t tmem_slot = bars + 8u * (2 * kMaxStages + 5);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 2 * kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, p.tmem_cols);       // one warp of each CTA, same columns in both
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = ld_shared_u32(tmem_slot);
+    const int64_t budget = p.timeout_ns;
+    const int64_t cluster_id = blockIdx.x >> 1;
+    const int64_t nclusters = gridDim.x >> 1;
+    const int32_t half_bn = p.BN / 2;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t s = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;
+            bool skip_one = p.stall != 0;
+            bool ok = true;
+            for (int64_t t = cluster_id; t < p.total_tiles && ok; t += nclusters) {
+                int b, mb, nb;
+                decode_tile(p, t, b, mb, nb);
+                const int32_t m0 = mb * (2 * kBM) + (int32_t)rank * kBM;   // this CTA's A rows
+                const int32_t n0 = nb * p.BN + (int32_t)rank * half_bn;    // this CTA's B columns
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!mbar_wait(empty_bar(s), ph ^ 1u, budget)) {
+                        report_error(p.err, DEV_TIMEOUT_PRODUCER);
+                        ok = false;
+                        break;
+                    }
+                    if (skip_one) {
+                        skip_one = false;          // test hook: this stage never fills
+                    } else {
+                        const uint32_t st = base + s * p.stage_stride;
+                        const int32_t k0 = kb * kBK;
+                        const uint32_t fb = mapa_shared(full_bar(s), lead);
+                        if (rank == 0) {
+                            mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);   // both CTAs' bytes
+                            issued_mask |= 1u << s;
+                            issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                        }
+                        for (uint32_t j = 0; j < p.a_nbox; ++j) {
+                            const uint32_t dst = st + j * p.a_box_bytes;
+                            if (p.a_mn_major) tma_load_3d_pair(dst, &tmA, fb, m0 + 64 * j, k0, b);
+                            else tma_load_3d_pair(dst, &tmA, fb, k0, m0 + p.a_box_mn * j, b);
+                        }
+                        for (uint32_t j = 0; j < p.b_nbox; ++j) {
+                            const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
+                            if (p.b_mn_major) tma_load_3d_pair(dst, &tmB, fb, n0 + 64 * j, k0, b);
+                            else tma_load_3d_pair(dst, &tmB, fb, k0, n0 + p.b_box_mn * j, b);
+                        }
+                    }
+                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (rank == 0) {
+                // Every armed stage has received both CTAs' bytes (immediate when
+                // the MMA thread already consumed it).
+                for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
+                    if ((issued_mask >> q) & 1u) {
+                        if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
+                            report_error(p.err, DEV_TIMEOUT_TEARDOWN);
+                    }
+                }
+            } else if (!ok) {
+                // The odd CTA cannot observe the even CTA's barrier: after a
+                // timeout give its own loads in flight a bounded time to land.
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < 2000000ull) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            uint32_t s = 0, ph = 0;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = cluster_id; t < p.total_tiles && ok; t += nclusters, ++it) {
+                const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+                if (!mbar_wait(acce_bar(buf), aph ^ 1u, budget)) {
+                    report_error(p.err, DEV_TIMEOUT_MMA);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
+                for (int kb = 0; kb < p.num_k; ++kb) {
+                    if (!mbar_wait(full_bar(s), ph, budget)) {
+                        report_error(p.err, DEV_TIMEOUT_MMA);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = base + s * p.stage_stride;
+                    const uint32_t b_addr = a_addr + p.b_off;
+                    const uint64_t a_desc = p.a_desc_hi | (uint64_t)((a_addr >> 4) & 0x3FFFu);
+                    const uint64_t b_desc = p.b_desc_hi | (uint64_t)((b_addr >> 4) & 0x3FFFu);
+#pragma unroll
+                    for (int k = 0; k < kBK / kMmaK; ++k) {
+                        umma_f16_pair(d_tmem, a_desc + (uint64_t)((k * p.a_kstep) >> 4),
+                                      b_desc + (uint64_t)((k * p.b_kstep) >> 4), p.idesc, (kb | k) != 0);
+                    }
+                    umma_commit_pair_mc(empty_bar(s), (uint16_t)(3u << lead));   // both CTAs' stage s free
+                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(accf_bar(buf), (uint16_t)(3u << lead));       // both accumulators ready
+            }
+            umma_commit_pair_mc(drain_bar, (uint16_t)(1u << lead));
+            if (!mbar_wait(drain_bar, 0, budget)) report_error(p.err, DEV_TIMEOUT_TEARDOWN);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs)
+        const uint32_t q = (uint32_t)warp & 3u;
+        const uint32_t lane_field = (q * 32u) << 16;
+        uint32_t it = 0, sbuf = 0;
+        for (int64_t t = cluster_id; t < p.total_tiles; t += nclusters, ++it) {
+            int b, mb, nb;
+            decode_tile(p, t, b, mb, nb);
+            const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+            int good = 1;
+            if (lane == 0) good = mbar_wait(accf_bar(buf), aph, budget) ? 1 : 0;
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                if (lane == 0) report_error(p.err, DEV_TIMEOUT_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int32_t m0 = mb * (2 * kBM) + (int32_t)rank * kBM + (int32_t)q * kEpiRowsPerWarp;
+            const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
+            const uint32_t acce = mapa_shared(acce_bar(buf), lead);
+            epilogue_tile<OUT>(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane, m0,
+                               nb * p.BN, b, [&] { mbar_arrive_cluster(acce); });
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, p.tmem_cols);
+}
+
+}  // namespace smo

@@ -151,7 +151,7 @@ uint32_t make_idesc(int in_dtype, int a_mn_major, int b_mn_major, int M, int N) 
 }
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
-               int out_dtype, int64_t batch, int num_sms, int force_bn) {
+               int out_dtype, int64_t batch, int num_sms, int force) {
     Plan p;
     p.M = M; p.N = N; p.K = K; p.batch = batch;
     p.in_dtype = in_dtype; p.out_dtype = out_dtype;
@@ -160,28 +160,34 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
         p.why = "dimension beyond 2^31-1";
         return p;
     }
-    p.num_m = (int)((M + kBM - 1) / kBM);
     p.num_k = (int)((K + kBK - 1) / kBK);
-    auto tiles_for = [&](int bn) { return (int64_t)p.num_m * ((N + bn - 1) / bn) * batch; };
-    int bn = 256;
-    if (force_bn == 128 || force_bn == 256) {
-        bn = force_bn;
-    } else {
-        // Wave quantisation: a 128-wide tile costs a bit over half a 256-wide one.
-        int64_t t256 = tiles_for(256), t128 = tiles_for(128);
-        double c256 = (double)((t256 + p.num_sms - 1) / p.num_sms) * 1.0;
-        double c128 = (double)((t128 + p.num_sms - 1) / p.num_sms) * 0.55;
-        bn = (c128 < c256) ? 128 : 256;
-    }
+    auto tiles_for = [&](int tm, int bn) { return ((M + tm - 1) / tm) * ((N + bn - 1) / bn) * batch; };
+    // Wave quantisation, in units of one 128 x 256 tile on one SM: a 128-wide
+    // tile costs a bit over half of that; a CTA pair computes a 256 x 256 tile
+    // on two SMs in about 0.85 of it (half the B bytes per SM, deeper pipeline).
+    const int64_t clusters = std::max(1, p.num_sms / 2);
+    const int64_t t256 = tiles_for(kBM, 256), t128 = tiles_for(kBM, 128), tpair = tiles_for(2 * kBM, 256);
+    const double c256 = (double)((t256 + p.num_sms - 1) / p.num_sms) * 1.0;
+    const double c128 = (double)((t128 + p.num_sms - 1) / p.num_sms) * 0.55;
+    const double cpair = (double)((tpair + clusters - 1) / clusters) * 0.85;
+    int choice;
+    if (force == 128 || force == 256 || force == 512) choice = force;
+    else if (cpair <= c256 && cpair <= c128) choice = 512;
+    else choice = (c128 < c256) ? 128 : 256;
+    p.pair = choice == 512;
+    p.tile_m = p.pair ? 2 * kBM : kBM;
+    const int bn = p.pair ? 256 : choice;
     p.BN = bn;
+    p.num_m = (int)((M + p.tile_m - 1) / p.tile_m);
     p.num_n = (int)((N + bn - 1) / bn);
-    p.tiles = tiles_for(bn);
-    p.grid = (int)std::min<int64_t>(p.tiles, p.num_sms);
-    p.group_m = std::min(16, p.num_m);
-    p.idesc = make_idesc(in_dtype, a_major, b_major, kBM, bn);
+    p.tiles = tiles_for(p.tile_m, bn);
+    p.grid = p.pair ? (int)(2 * std::min<int64_t>(p.tiles, clusters)) : (int)std::min<int64_t>(p.tiles, p.num_sms);
+    p.group_m = std::min(p.pair ? 8 : 16, p.num_m);
+    p.idesc = make_idesc(in_dtype, a_major, b_major, p.tile_m, bn);
 
+    // Per-CTA operand tiles: A 128 rows; B all BN columns, or half of them in a pair.
     plan_operand(p.a, a_major, kBM);
-    plan_operand(p.b, b_major, bn);
+    plan_operand(p.b, b_major, p.pair ? bn / 2 : bn);
 
     p.c.out_es = (out_dtype == 2) ? 4 : 2;
     p.c.chunk_cols = 128 / p.c.out_es;
@@ -256,7 +262,7 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->b_off = p.a.stage_bytes;
     kp->off_epi = p.off_epi; kp->off_bar = p.off_bar;
     kp->tmem_cols = p.tmem_cols;
-    kp->tx_bytes = p.stage_stride;
+    kp->tx_bytes = p.pair ? 2 * p.stage_stride : p.stage_stride;   // a pair's even CTA arms both CTAs' bytes
     kp->epi_chunk_cols = p.c.chunk_cols;
     kp->epi_chunks = p.c.chunks;
 }
@@ -280,7 +286,7 @@ std::string describe_json(const Plan& p) {
     };
     o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
       << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
-      << ",\"BM\":" << kBM << ",\"BN\":" << p.BN << ",\"BK\":" << kBK << ",\"mma_k\":" << kMmaK
+      << ",\"pair\":" << p.pair << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << kBK << ",\"mma_k\":" << kMmaK
       << ",\"stages\":" << p.stages << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
       << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads

@@ -44,6 +44,8 @@ struct EpiPlan {
 struct Plan {
     int64_t M = 0, N = 0, K = 0, batch = 1;
     int in_dtype = 0, out_dtype = 0;
+    int pair = 0;                   // 1: CTA pair (cta_group::2), 256 x BN tiles over two SMs
+    int tile_m = 128;               // output rows per tile (128, or 256 for a pair)
     int BN = 256, stages = 4;
     int num_m = 0, num_n = 0, num_k = 0, group_m = 16;
     int64_t tiles = 0;
@@ -57,9 +59,9 @@ struct Plan {
 };
 
 // in_dtype: 0 bf16, 1 f16.  out_dtype: 0 bf16, 1 f16, 2 f32 (gemm_dtype_t).
-// force_bn: 0 = choose, else 128 or 256.
+// force: 0 = choose; 128 or 256 = one CTA with that BN; 512 = CTA pair (256 x 256).
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
-               int out_dtype, int64_t batch, int num_sms, int force_bn);
+               int out_dtype, int64_t batch, int num_sms, int force);
 
 // Fills the kernel parameter block from a plan (pointers and runtime knobs are
 // set by the caller).

@@ -95,8 +95,9 @@ def test_planner_layouts_match_oracle(lib, am, bm, out):
         assert d["ok"], d["why"]
         assert d["smem_bytes"] <= 232448
         assert d["tmem_cols"] == 2 * d["BN"] and d["tmem_cols"] <= 512
-        for name, major, tile in (("A", am, d["BM"]), ("B", bm, d["BN"])):
+        for name, major in (("A", am), ("B", bm)):
             op = d[name]
+            tile = op["tile_mn"]          # per-CTA operand tile (half of BN in a pair)
             mn_major = bool(major)
             # planner's F2 basis images == oracle's 128B-swizzle TMA box layout
             want_mn = [banksim.operand_tile_offset(1 << i, 0, mn_major, tile)
@@ -150,14 +151,27 @@ def test_instruction_descriptor_fields(lib):
                 assert (x >> 7) & 7 == fmt and (x >> 10) & 7 == fmt
                 assert (x >> 15) & 1 == am and (x >> 16) & 1 == bm
                 assert ((x >> 17) & 63) * 8 == d["BN"]
-                assert ((x >> 24) & 31) * 16 == 128
+                assert ((x >> 24) & 31) * 16 == d["BM"]
                 assert x & 0b1111 == 0 and (x >> 13) & 3 == 0 and (x >> 23) & 1 == 0
 
 
 def test_tile_choice_and_grid(lib):
     d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
-    assert d["BN"] == 128 and d["tiles"] == 12 * 9 and d["grid"] == 108
+    assert not d["pair"] and d["BN"] == 128 and d["tiles"] == 12 * 9 and d["grid"] == 108
     d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
-    assert d["BN"] == 256 and d["tiles"] == 64 * 32 and d["grid"] == 152
+    assert d["pair"] and d["BM"] == 256 and d["BN"] == 256 and d["tiles"] == 32 * 32
+    assert d["grid"] == 152 and d["stages"] == 6 and d["A"]["tile_mn"] == d["B"]["tile_mn"] == 128
     d = smo.gemm_plan_describe(2048, 2048, 2048, 0, 1, "bf16", "bf16", batch=32)
-    assert d["tiles"] == 16 * 8 * 32
+    assert d["pair"] and d["tiles"] == 8 * 8 * 32
+
+
+def test_pair_descriptors(lib):
+    """CTA pair: M = 256 and N = 256 in the instruction descriptor, each CTA
+    stages 128 rows of A and 128 columns of B per 64-deep stage."""
+    for am in (0, 1):
+        for bm in (0, 1):
+            d = smo.gemm_plan_describe(8192, 8192, 8192, am, bm, "bf16", "bf16")
+            x = d["idesc"]
+            assert ((x >> 24) & 31) * 16 == 256 and ((x >> 17) & 63) * 8 == 256
+            assert d["stage_stride"] == 2 * 128 * 64 * 2
+            assert d["tmem_cols"] == 512

@@ -30,6 +30,62 @@ def _full(p, exact=False, stream=None):
     return check(p, gpu, oracle_full(p), exact=exact)
 
 
+@pytest.fixture
+def force_mode(monkeypatch):
+    """Force one tile mode of the planner (128 / 256: one CTA with that BN;
+    512: CTA pair with 256 x 256 tiles)."""
+    def _set(mode):
+        monkeypatch.setenv("SMO_GEMM_FORCE_BN", str(mode))
+    yield _set
+
+
+# ------------------------------------------------------------ every tile mode
+@pytest.mark.parametrize("mode", [128, 256, 512])
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_tile_modes_ragged(force_mode, mode, am, bm):
+    force_mode(mode)
+    for (M, N, K, out) in [(256, 256, 64, "f32"), (600, 700, 300, "bf16"), (257, 513, 129, "f32"),
+                           (1, 8, 16, "bf16"), (520, 1030, 1000, "f16")]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="f16" if out == "f16" else "bf16",
+                         out_dtype=out, dist="uniform", seed=M + K + mode)
+        _full(p)
+
+
+@pytest.mark.parametrize("mode", [128, 256, 512])
+def test_tile_modes_integer_and_permutation_exact(force_mode, mode):
+    force_mode(mode)
+    for am, bm in MAJORS:
+        p = make_problem(384, 640, 448, a_major=am, b_major=bm, dist="int", seed=mode,
+                         out_dtype="f32")
+        _full(p, exact=True)
+        q = make_problem(512, 512, 256, a_major=am, b_major=bm, dist="uniform", seed=1)
+        g = torch.Generator().manual_seed(mode + am * 2 + bm)
+        perm = torch.randperm(256, generator=g)
+        P = torch.zeros(512, 256)
+        P[torch.arange(512), perm[torch.arange(512) % 256]] = 1.0
+        q.logical_A()[0].copy_(P.to(torch.bfloat16))
+        _full(q, exact=True)
+
+
+@pytest.mark.parametrize("mode", [128, 256, 512])
+def test_tile_modes_batched_and_timeout(force_mode, mode):
+    force_mode(mode)
+    p = make_problem(300, 260, 200, batch=3, dist="normal", sigma=0.5, seed=4, out_dtype="bf16")
+    _full(p)
+    old = smo.gemm_set_timeout_ns(20_000_000)
+    try:
+        smo.gemm_debug_inject_stall(True)
+        A = torch.zeros(512, 512, dtype=torch.bfloat16, device="cuda")
+        C = torch.zeros(512, 512, dtype=torch.float32, device="cuda")
+        smo.gemm_ex(A, 512, 0, A, 512, 1, C, 512, 512, 512, 512, out_dtype="f32")
+        assert smo.gemm_check() == smo.GEMM_ERR_TIMEOUT
+    finally:
+        smo.gemm_debug_inject_stall(False)
+        smo.gemm_set_timeout_ns(old)
+    assert smo.gemm_check() == smo.GEMM_OK
+    _full(make_problem(256, 256, 256, dist="uniform", out_dtype="f32"))
+
+
 # ------------------------------------------------------------ small / ragged
 @pytest.mark.parametrize("am,bm", MAJORS)
 @pytest.mark.parametrize("ind,out", [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f32"), ("f16", "f16")])
