@@ -139,6 +139,24 @@ int encode(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t out
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
 }
 
+// 4-D map for an MN-major operand whose per-stage boxes are loaded by one
+// instruction: dims {64 (contiguous), K, MN / 64, batch}; needs MN % 64 == 0 so
+// that no box reaches past the operand's extent.
+int encode4(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t k, uint64_t batch, uint64_t ld,
+            uint64_t stride, uint32_t nbox) {
+    const uint64_t es = (uint64_t)elem_size(dt);
+    cuuint64_t dims[4] = {64, k, mn / 64, batch};
+    uint64_t bstride = stride * es;
+    if (batch <= 1) bstride = ((ld * es * k + 15) / 16) * 16;
+    cuuint64_t strides[3] = {ld * es, 64 * es, bstride};
+    cuuint32_t box[4] = {64, (cuuint32_t)smo::kBK, nbox, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, tmap_type(dt), 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
+}
+
 template <int OUT>
 int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
                   const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
@@ -261,27 +279,39 @@ int noalloc_state(NoAllocState** out) {
     return GEMM_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C, int64_t ldc,
-            int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int64_t batch, int64_t strideA,
-            int64_t strideB, int64_t strideC, void* stream_) {
+// Argument checks of gemm_ex / gemm_ex_noalloc.  Returns GEMM_OK to proceed,
+// 1 when there is nothing to launch (empty product), or an error status.
+int check_args(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C,
+               int64_t ldc, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int64_t batch,
+               int64_t strideA, int64_t strideB, int64_t strideC) {
     int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
     if (st != GEMM_OK) return st;
-    if (M == 0 || N == 0) return GEMM_OK;
+    if (M == 0 || N == 0) return 1;
     if (!C) return GEMM_ERR_ARG;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     const int64_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
     if (ldc < N) return GEMM_ERR_ARG;
     if (batch > 1 && strideC < (M - 1) * ldc + N) return GEMM_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc * oes) % 16 || (batch > 1 && (strideC * oes) % 16))
         return GEMM_ERR_ALIGN;
-    DevState* ds = nullptr;
+    if (K == 0) return GEMM_OK;
+    if (!A || !B) return GEMM_ERR_ARG;
+    const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
+    const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
+    if (lda < a_row || ldb < b_row) return GEMM_ERR_ARG;
+    if (batch > 1 && (strideA < 1 || strideB < 1)) return GEMM_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda * ies) % 16 ||
+        (ldb * ies) % 16 || (batch > 1 && ((strideA * ies) % 16 || (strideB * ies) % 16)))
+        return GEMM_ERR_ALIGN;
+    return GEMM_OK;
+}
+
+// Plans, encodes the tensor maps and launches, for already-checked arguments
+// on a device whose state `ds` is ready; `err` is the kernel's error word.
+int run_gemm(DevState& ds, int32_t* err, const void* A, int64_t lda, int a_major, const void* B, int64_t ldb,
+             int b_major, void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype,
+             int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC, cudaStream_t stream) {
+    const int64_t oes = elem_size(out_dtype);
     if (K == 0) {
-        st = device_state(&ds);
-        if (st != GEMM_OK) return st;
         for (int64_t b = 0; b < batch; ++b) {
             char* cb = static_cast<char*>(C) + b * (batch > 1 ? strideC : 0) * oes;
             if (cudaMemset2DAsync(cb, (size_t)(ldc * oes), 0, (size_t)(N * oes), (size_t)M, stream) !=
@@ -292,28 +322,27 @@ int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb,
         }
         return GEMM_OK;
     }
-    if (!A || !B) return GEMM_ERR_ARG;
-    const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
-    const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
-    if (lda < a_row || ldb < b_row) return GEMM_ERR_ARG;
-    if (batch > 1 && (strideA < 1 || strideB < 1)) return GEMM_ERR_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda * ies) % 16 ||
-        (ldb * ies) % 16 || (batch > 1 && ((strideA * ies) % 16 || (strideB * ies) % 16)))
-        return GEMM_ERR_ALIGN;
-
-    st = device_state(&ds);
-    if (st != GEMM_OK) return st;
-    const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, ds->num_sms);
+    const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, ds.num_sms);
     if (!pl->ok) return GEMM_ERR_UNSUPPORTED;
 
     // TMA stores write whole 16-byte pieces, so the C map covers only the
     // 16-byte-aligned prefix of each row; the kernel stores the rest directly.
     const int64_t n_tma = (N * oes / 16) * 16 / oes;
-    CUtensorMap ta, tb, tc;
+    const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
+    const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
     const int64_t a_outer = (a_major == GEMM_MN_MAJOR) ? K : M;
     const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
-    if (encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer) ||
-        encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer) ||
+    CUtensorMap ta, tb, tc;
+    // MN-major operands whose extent is a multiple of 64 take one 4-D load per
+    // stage instead of one load per 64-wide box.
+    const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % 64 == 0 &&
+                         encode4(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox) == GEMM_OK;
+    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % 64 == 0 &&
+                         encode4(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox) == GEMM_OK;
+    if ((!a_fused &&
+         encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer)) ||
+        (!b_fused &&
+         encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer)) ||
         encode(&tc, out_dtype, C, (uint64_t)(n_tma > 0 ? n_tma : 16 / oes), M, batch, ldc, strideC,
                (uint32_t)pl->c.chunk_cols, (uint32_t)smo::kEpiRowsPerWarp))
         return GEMM_ERR_UNSUPPORTED;
@@ -321,19 +350,39 @@ int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb,
     KParams kp;
     std::memset(&kp, 0, sizeof(kp));
     smo::fill_params(*pl, &kp);
+    kp.a_fused = a_fused ? 1u : 0u;
+    kp.b_fused = b_fused ? 1u : 0u;
     kp.C = C;
     kp.ldc = ldc;
     kp.strideC = batch > 1 ? strideC : 0;
     kp.n_tma = (int32_t)n_tma;
-    kp.err = ds->d_err;
+    kp.err = err;
     kp.timeout_ns = g_timeout_ns.load();
     kp.stall = g_stall.load();
 
     switch (out_dtype) {
-        case GEMM_F32: return launch<smo::OUT_F32>(*pl, *ds, ta, tb, tc, kp, stream);
-        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, *ds, ta, tb, tc, kp, stream);
-        default: return launch<smo::OUT_F16>(*pl, *ds, ta, tb, tc, kp, stream);
+        case GEMM_F32: return launch<smo::OUT_F32>(*pl, ds, ta, tb, tc, kp, stream);
+        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, ds, ta, tb, tc, kp, stream);
+        default: return launch<smo::OUT_F16>(*pl, ds, ta, tb, tc, kp, stream);
     }
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C, int64_t ldc,
+            int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype, int64_t batch, int64_t strideA,
+            int64_t strideB, int64_t strideC, void* stream_) {
+    int st = check_args(A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype, out_dtype, batch, strideA,
+                        strideB, strideC);
+    if (st == 1) return GEMM_OK;
+    if (st != GEMM_OK) return st;
+    DevState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != GEMM_OK) return st;
+    return run_gemm(*ds, ds->d_err, A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype, out_dtype, batch,
+                    strideA, strideB, strideC, reinterpret_cast<cudaStream_t>(stream_));
 }
 
 int gemm_bf16(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C,
@@ -404,77 +453,22 @@ int gemm_ex_noalloc(const void* A, int64_t lda, int a_major, const void* B, int6
     // Sizes: the scratch this variant needs is one word whatever the problem
     // size; problems beyond the library's limits (any dimension or batch
     // >= 2^31) are rejected here with GEMM_ERR_UNSUPPORTED.
-    int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
+    int st = check_args(A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype, out_dtype, batch, strideA,
+                        strideB, strideC);
+    if (st == 1) return GEMM_OK;
     if (st != GEMM_OK) return st;
-    if (M == 0 || N == 0) return GEMM_OK;
-    if (!C) return GEMM_ERR_ARG;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const int64_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
-    if (ldc < N) return GEMM_ERR_ARG;
-    if (batch > 1 && strideC < (M - 1) * ldc + N) return GEMM_ERR_ARG;
-    if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc * oes) % 16 || (batch > 1 && (strideC * oes) % 16))
-        return GEMM_ERR_ALIGN;
     NoAllocState* na = nullptr;
-    if (K == 0) {
-        st = noalloc_state(&na);
-        if (st != GEMM_OK) return st;
-        for (int64_t b = 0; b < batch; ++b) {
-            char* cb = static_cast<char*>(C) + b * (batch > 1 ? strideC : 0) * oes;
-            if (cudaMemset2DAsync(cb, (size_t)(ldc * oes), 0, (size_t)(N * oes), (size_t)M, stream) !=
-                cudaSuccess) {
-                cudaGetLastError();
-                return GEMM_ERR_LAUNCH;
-            }
-        }
-        return GEMM_OK;
-    }
-    if (!A || !B) return GEMM_ERR_ARG;
-    const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
-    const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
-    if (lda < a_row || ldb < b_row) return GEMM_ERR_ARG;
-    if (batch > 1 && (strideA < 1 || strideB < 1)) return GEMM_ERR_ARG;
-    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) || (lda * ies) % 16 ||
-        (ldb * ies) % 16 || (batch > 1 && ((strideA * ies) % 16 || (strideB * ies) % 16)))
-        return GEMM_ERR_ALIGN;
-
     st = noalloc_state(&na);
     if (st != GEMM_OK) return st;
-    const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, na->ds.num_sms);
-    if (!pl->ok) return GEMM_ERR_UNSUPPORTED;
-
-    const int64_t n_tma = (N * oes / 16) * 16 / oes;
-    CUtensorMap ta, tb, tc;
-    const int64_t a_outer = (a_major == GEMM_MN_MAJOR) ? K : M;
-    const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
-    if (encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer) ||
-        encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer) ||
-        encode(&tc, out_dtype, C, (uint64_t)(n_tma > 0 ? n_tma : 16 / oes), M, batch, ldc, strideC,
-               (uint32_t)pl->c.chunk_cols, (uint32_t)smo::kEpiRowsPerWarp))
-        return GEMM_ERR_UNSUPPORTED;
-
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     // The shared array keeps the previous call's contents: the error word must
     // start at zero for this launch (memset on the stream, no allocation).
-    if (cudaMemsetAsync(na->scratch, 0, sizeof(int32_t), stream) != cudaSuccess) {
+    if (K > 0 && cudaMemsetAsync(na->scratch, 0, sizeof(int32_t), stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-
-    KParams kp;
-    std::memset(&kp, 0, sizeof(kp));
-    smo::fill_params(*pl, &kp);
-    kp.C = C;
-    kp.ldc = ldc;
-    kp.strideC = batch > 1 ? strideC : 0;
-    kp.n_tma = (int32_t)n_tma;
-    kp.err = na->scratch;
-    kp.timeout_ns = g_timeout_ns.load();
-    kp.stall = g_stall.load();
-
-    switch (out_dtype) {
-        case GEMM_F32: return launch<smo::OUT_F32>(*pl, na->ds, ta, tb, tc, kp, stream);
-        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, na->ds, ta, tb, tc, kp, stream);
-        default: return launch<smo::OUT_F16>(*pl, na->ds, ta, tb, tc, kp, stream);
-    }
+    return run_gemm(na->ds, na->scratch, A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype, out_dtype,
+                    batch, strideA, strideB, strideC, stream);
 }
 
 }  // extern "C"

@@ -97,20 +97,20 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
         }
         if (nc + kChunkCols > p.n_tma && nc < p.N) {
             // TMA stores write whole 16-byte pieces at the row end; the last
-            // < 16 bytes of a ragged row are stored from registers.
+            // < 16 bytes of a ragged row are copied from this lane's own row of
+            // the swizzled slab (its own st.shared above are visible to it).
             const int32_t m = m0 + lane;
             if (m < p.M) {
                 char* rowp = static_cast<char*>(p.C) + ((int64_t)b * p.strideC + (int64_t)m * p.ldc) * kOutBytes;
-#pragma unroll
-                for (int i = 0; i < kChunkCols; ++i) {
-                    const int32_t n = nc + i;
-                    if (n >= p.n_tma && n < p.N) {
-                        if (OUT == OUT_F32)
-                            *reinterpret_cast<uint32_t*>(rowp + (int64_t)n * 4) = v[i];
-                        else
-                            *reinterpret_cast<uint16_t*>(rowp + (int64_t)n * 2) =
-                                (uint16_t)(v[i >> 1] >> (16 * (i & 1)));
-                    }
+                const int32_t n_lo = max(p.n_tma, nc), n_hi = min(p.N, nc + kChunkCols);
+#pragma unroll 1
+                for (int32_t n = n_lo; n < n_hi; ++n) {
+                    const uint32_t byte = (uint32_t)(n - nc) * kOutBytes;
+                    const uint32_t src = row + ((((byte >> 4) ^ (uint32_t)(lane & 7)) << 4) | (byte & 15u));
+                    if (OUT == OUT_F32)
+                        *reinterpret_cast<uint32_t*>(rowp + (int64_t)n * 4) = ld_shared_u32(src);
+                    else
+                        *reinterpret_cast<uint16_t*>(rowp + (int64_t)n * 2) = ld_shared_u16(src);
                 }
             }
         }

@@ -104,15 +104,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t st = base + s * p.stage_stride;
                         const int32_t k0 = kb * kBK;
                         mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
-                        for (uint32_t j = 0; j < p.a_nbox; ++j) {
-                            const uint32_t dst = st + j * p.a_box_bytes;
-                            if (p.a_mn_major) tma_load_3d(dst, &tmA, full_bar(s), m0 + 64 * j, k0, b);
-                            else tma_load_3d(dst, &tmA, full_bar(s), k0, m0 + p.a_box_mn * j, b);
+                        if (p.a_fused) {
+                            tma_load_4d(st, &tmA, full_bar(s), 0, k0, m0 / 64, b);
+                        } else {
+                            for (uint32_t j = 0; j < p.a_nbox; ++j) {
+                                const uint32_t dst = st + j * p.a_box_bytes;
+                                if (p.a_mn_major) tma_load_3d(dst, &tmA, full_bar(s), m0 + 64 * j, k0, b);
+                                else tma_load_3d(dst, &tmA, full_bar(s), k0, m0 + p.a_box_mn * j, b);
+                            }
                         }
-                        for (uint32_t j = 0; j < p.b_nbox; ++j) {
-                            const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
-                            if (p.b_mn_major) tma_load_3d(dst, &tmB, full_bar(s), n0 + 64 * j, k0, b);
-                            else tma_load_3d(dst, &tmB, full_bar(s), k0, n0 + p.b_box_mn * j, b);
+                        if (p.b_fused) {
+                            tma_load_4d(st + p.b_off, &tmB, full_bar(s), 0, k0, n0 / 64, b);
+                        } else {
+                            for (uint32_t j = 0; j < p.b_nbox; ++j) {
+                                const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
+                                if (p.b_mn_major) tma_load_3d(dst, &tmB, full_bar(s), n0 + 64 * j, k0, b);
+                                else tma_load_3d(dst, &tmB, full_bar(s), k0, n0 + p.b_box_mn * j, b);
+                            }
                         }
                         issued_mask |= 1u << s;
                         issued_ph = (issued_ph & ~(1u << s)) | (ph << s);

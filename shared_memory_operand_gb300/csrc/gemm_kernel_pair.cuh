@@ -108,15 +108,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             issued_mask |= 1u << s;
                             issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                         }
-                        for (uint32_t j = 0; j < p.a_nbox; ++j) {
-                            const uint32_t dst = st + j * p.a_box_bytes;
-                            if (p.a_mn_major) tma_load_3d_pair(dst, &tmA, fb, m0 + 64 * j, k0, b);
-                            else tma_load_3d_pair(dst, &tmA, fb, k0, m0 + p.a_box_mn * j, b);
+                        if (p.a_fused) {
+                            tma_load_4d_pair(st, &tmA, fb, 0, k0, m0 / 64, b);
+                        } else {
+                            for (uint32_t j = 0; j < p.a_nbox; ++j) {
+                                const uint32_t dst = st + j * p.a_box_bytes;
+                                if (p.a_mn_major) tma_load_3d_pair(dst, &tmA, fb, m0 + 64 * j, k0, b);
+                                else tma_load_3d_pair(dst, &tmA, fb, k0, m0 + p.a_box_mn * j, b);
+                            }
                         }
-                        for (uint32_t j = 0; j < p.b_nbox; ++j) {
-                            const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
-                            if (p.b_mn_major) tma_load_3d_pair(dst, &tmB, fb, n0 + 64 * j, k0, b);
-                            else tma_load_3d_pair(dst, &tmB, fb, k0, n0 + p.b_box_mn * j, b);
+                        if (p.b_fused) {
+                            tma_load_4d_pair(st + p.b_off, &tmB, fb, 0, k0, n0 / 64, b);
+                        } else {
+                            for (uint32_t j = 0; j < p.b_nbox; ++j) {
+                                const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
+                                if (p.b_mn_major) tma_load_3d_pair(dst, &tmB, fb, n0 + 64 * j, k0, b);
+                                else tma_load_3d_pair(dst, &tmB, fb, k0, n0 + p.b_box_mn * j, b);
+                            }
                         }
                     }
                     if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }

@@ -38,6 +38,7 @@ struct KParams {
     uint32_t idesc;                 // tcgen05 instruction descriptor
     uint32_t a_mn_major, b_mn_major;
     uint32_t a_nbox, b_nbox;        // TMA boxes per stage and operand
+    uint32_t a_fused, b_fused;      // 1: an MN-major operand's boxes come from one 4-D TMA load
     uint32_t a_box_bytes, b_box_bytes;
     uint32_t a_box_mn, b_box_mn;    // MN extent of one box
     uint32_t a_kstep, b_kstep;      // descriptor start-address advance per 16-wide K step (bytes)

@@ -44,8 +44,11 @@ def force_mode(monkeypatch):
 @pytest.mark.parametrize("am,bm", MAJORS)
 def test_tile_modes_ragged(force_mode, mode, am, bm):
     force_mode(mode)
+    # (192, 320): MN extents multiple of 64 but not of the tile (one-instruction
+    # 4-D operand loads whose last 64-wide box is out of range)
     for (M, N, K, out) in [(256, 256, 64, "f32"), (600, 700, 300, "bf16"), (257, 513, 129, "f32"),
-                           (1, 8, 16, "bf16"), (520, 1030, 1000, "f16")]:
+                           (1, 8, 16, "bf16"), (520, 1030, 1000, "f16"), (192, 320, 128, "bf16"),
+                           (64, 704, 96, "f32")]:
         p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="f16" if out == "f16" else "bf16",
                          out_dtype=out, dist="uniform", seed=M + K + mode)
         _full(p)
