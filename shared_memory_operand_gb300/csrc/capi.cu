@@ -121,16 +121,17 @@ const Plan* cached_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_majo
     return &(g_plans[key] = p);
 }
 
-// 3-D tiled tensor map: dims {inner, outer, batch}, 128-byte swizzle.
-int encode(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint64_t batch, uint64_t ld,
-           uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+uint64_t batch_stride_bytes(uint64_t es, uint64_t ld, uint64_t outer, uint64_t batch, uint64_t stride) {
+    // extent-1 batch dimension: any valid stride (multiple of 16 bytes)
+    return batch <= 1 ? ((ld * es * outer + 15) / 16) * 16 : stride * es;
+}
+
+// C: 3-D tiled map {N, M, batch}, 128-byte swizzle (TMA stores).
+int encode_c(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint64_t batch, uint64_t ld,
+             uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
     const uint64_t es = (uint64_t)elem_size(dt);
     cuuint64_t dims[3] = {inner, outer, batch};
-    uint64_t bstride = stride * es;
-    if (batch <= 1) {
-        bstride = ((ld * es * outer + 15) / 16) * 16;   // unused extent-1 dimension
-    }
-    cuuint64_t strides[2] = {ld * es, bstride};
+    cuuint64_t strides[2] = {ld * es, batch_stride_bytes(es, ld, outer, batch, stride)};
     cuuint32_t box[3] = {box_inner, box_outer, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, tmap_type(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -139,16 +140,30 @@ int encode(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t out
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
 }
 
-// 4-D map for an MN-major operand whose per-stage boxes are loaded by one
-// instruction: dims {64 (contiguous), K, MN / 64, batch}; needs MN % 64 == 0 so
-// that no box reaches past the operand's extent.
-int encode4(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t k, uint64_t batch, uint64_t ld,
-            uint64_t stride, uint32_t nbox) {
+// Operand box map, 4-D so that every load of a stage uses the same TMA
+// instruction form: {inner, outer, 1, batch}.
+int encode_box(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t outer, uint64_t batch, uint64_t ld,
+               uint64_t stride, uint32_t box_inner, uint32_t box_outer) {
+    const uint64_t es = (uint64_t)elem_size(dt);
+    const uint64_t one = ((ld * es * outer + 15) / 16) * 16;
+    cuuint64_t dims[4] = {inner, outer, 1, batch};
+    cuuint64_t strides[3] = {ld * es, one, batch_stride_bytes(es, ld, outer, batch, stride)};
+    cuuint32_t box[4] = {box_inner, box_outer, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, tmap_type(dt), 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
+}
+
+// MN-major operand whose per-stage boxes are loaded by one instruction:
+// {64 (contiguous), K, MN / 64, batch}; needs MN % 64 == 0 so that no box
+// reaches past the operand's extent.
+int encode_fused(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t k, uint64_t batch, uint64_t ld,
+                 uint64_t stride, uint32_t nbox) {
     const uint64_t es = (uint64_t)elem_size(dt);
     cuuint64_t dims[4] = {64, k, mn / 64, batch};
-    uint64_t bstride = stride * es;
-    if (batch <= 1) bstride = ((ld * es * k + 15) / 16) * 16;
-    cuuint64_t strides[3] = {ld * es, 64 * es, bstride};
+    cuuint64_t strides[3] = {ld * es, 64 * es, batch_stride_bytes(es, ld, k, batch, stride)};
     cuuint32_t box[4] = {64, (cuuint32_t)smo::kBK, nbox, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, tmap_type(dt), 4, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -336,14 +351,14 @@ int run_gemm(DevState& ds, int32_t* err, const void* A, int64_t lda, int a_major
     // MN-major operands whose extent is a multiple of 64 take one 4-D load per
     // stage instead of one load per 64-wide box.
     const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % 64 == 0 &&
-                         encode4(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox) == GEMM_OK;
+                         encode_fused(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox) == GEMM_OK;
     const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % 64 == 0 &&
-                         encode4(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox) == GEMM_OK;
+                         encode_fused(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox) == GEMM_OK;
     if ((!a_fused &&
-         encode(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer)) ||
+         encode_box(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer)) ||
         (!b_fused &&
-         encode(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer)) ||
-        encode(&tc, out_dtype, C, (uint64_t)(n_tma > 0 ? n_tma : 16 / oes), M, batch, ldc, strideC,
+         encode_box(&tb, in_dtype, B, b_row, b_outer, batch, ldb, strideB, pl->b.box_inner, pl->b.box_outer)) ||
+        encode_c(&tc, out_dtype, C, (uint64_t)(n_tma > 0 ? n_tma : 16 / oes), M, batch, ldc, strideC,
                (uint32_t)pl->c.chunk_cols, (uint32_t)smo::kEpiRowsPerWarp))
         return GEMM_ERR_UNSUPPORTED;
 

@@ -30,6 +30,53 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int64_t t, int& b,
     nb = rr / gsz;
 }
 
+// One TMA load of a pipeline stage, owned by one lane of the producer warp.
+// All of a stage's loads (A boxes, then B boxes) are issued by consecutive
+// lanes in a single instruction: the producer's issue cost is then one
+// instruction per stage instead of one per box.  Every operand map is 4-D:
+//   fused MN-major (extent % 64 == 0): {64, K, MN / 64, batch}, one load
+//   K-major box:                       {K, MN, 1, batch}
+//   MN-major 64-wide box:              {MN, K, 1, batch}
+struct LoadSlot {
+    const CUtensorMap* tm;
+    uint32_t dst_off;      // from the stage base
+    uint32_t mode;         // 0 fused, 1 K-major box, 2 MN-major box
+    int32_t mn_off;        // offset of this box along MN
+    bool is_a;
+};
+
+__device__ __forceinline__ uint32_t stage_loads(const KParams& p) {
+    return (p.a_fused ? 1u : p.a_nbox) + (p.b_fused ? 1u : p.b_nbox);
+}
+
+__device__ __forceinline__ LoadSlot load_slot(const KParams& p, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                              uint32_t lane) {
+    const uint32_t na = p.a_fused ? 1u : p.a_nbox;
+    LoadSlot s;
+    s.is_a = lane < na;
+    const uint32_t j = s.is_a ? lane : lane - na;
+    const uint32_t fused = s.is_a ? p.a_fused : p.b_fused;
+    const uint32_t mn_major = s.is_a ? p.a_mn_major : p.b_mn_major;
+    s.tm = s.is_a ? tmA : tmB;
+    s.dst_off = (s.is_a ? 0u : p.b_off) + j * (s.is_a ? p.a_box_bytes : p.b_box_bytes);
+    s.mode = fused ? 0u : (mn_major ? 2u : 1u);
+    s.mn_off = (int32_t)(j * (s.is_a ? p.a_box_mn : p.b_box_mn));
+    return s;
+}
+
+// Coordinates of a slot's load for K block k0 of the tile whose operand rows
+// (A) / columns (B) start at mn0.
+__device__ __forceinline__ void slot_coords(const LoadSlot& s, int32_t mn0, int32_t k0, int32_t& c0, int32_t& c1,
+                                            int32_t& c2) {
+    if (s.mode == 0) {
+        c0 = 0; c1 = k0; c2 = mn0 / 64;
+    } else if (s.mode == 1) {
+        c0 = k0; c1 = mn0 + s.mn_off; c2 = 0;
+    } else {
+        c0 = mn0 + s.mn_off; c1 = k0; c2 = 0;
+    }
+}
+
 template <int OUT>
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     const float a = __uint_as_float(lo), b = __uint_as_float(hi);

@@ -83,18 +83,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
-        if (lane == 0) {
+        // Lanes 0 .. nloads-1 each own one load of every stage and issue them
+        // together; lane 0 waits for the free slot and arms the stage.
+        const uint32_t nloads = stage_loads(p);
+        if ((uint32_t)lane < nloads) {
+            const uint32_t lmask = (1u << nloads) - 1u;
+            const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
             uint32_t s = 0, ph = 0;
-            uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per stage
+            uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per stage (lane 0)
             bool skip_one = p.stall != 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
                 int b, mb, nb;
                 decode_tile(p, t, b, mb, nb);
-                const int32_t m0 = mb * kBM, n0 = nb * p.BN;
+                const int32_t mn0 = slot.is_a ? mb * kBM : nb * p.BN;
                 for (int kb = 0; kb < p.num_k; ++kb) {
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, budget)) {
-                        report_error(p.err, DEV_TIMEOUT_PRODUCER);
+                    int good = 1;
+                    if (lane == 0) good = mbar_wait(empty_bar(s), ph ^ 1u, budget) ? 1 : 0;
+                    good = __shfl_sync(lmask, good, 0);
+                    if (!good) {
+                        if (lane == 0) report_error(p.err, DEV_TIMEOUT_PRODUCER);
                         ok = false;
                         break;
                     }
@@ -102,38 +110,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         skip_one = false;          // test hook: this stage never fills
                     } else {
                         const uint32_t st = base + s * p.stage_stride;
-                        const int32_t k0 = kb * kBK;
-                        mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
-                        if (p.a_fused) {
-                            tma_load_4d(st, &tmA, full_bar(s), 0, k0, m0 / 64, b);
-                        } else {
-                            for (uint32_t j = 0; j < p.a_nbox; ++j) {
-                                const uint32_t dst = st + j * p.a_box_bytes;
-                                if (p.a_mn_major) tma_load_3d(dst, &tmA, full_bar(s), m0 + 64 * j, k0, b);
-                                else tma_load_3d(dst, &tmA, full_bar(s), k0, m0 + p.a_box_mn * j, b);
-                            }
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
+                            issued_mask |= 1u << s;
+                            issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                         }
-                        if (p.b_fused) {
-                            tma_load_4d(st + p.b_off, &tmB, full_bar(s), 0, k0, n0 / 64, b);
-                        } else {
-                            for (uint32_t j = 0; j < p.b_nbox; ++j) {
-                                const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
-                                if (p.b_mn_major) tma_load_3d(dst, &tmB, full_bar(s), n0 + 64 * j, k0, b);
-                                else tma_load_3d(dst, &tmB, full_bar(s), k0, n0 + p.b_box_mn * j, b);
-                            }
-                        }
-                        issued_mask |= 1u << s;
-                        issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                        __syncwarp(lmask);
+                        int32_t c0, c1, c2;
+                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
+                        tma_load_4d(st + slot.dst_off, slot.tm, full_bar(s), c0, c1, c2, b);
                     }
                     if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
                 }
             }
-            // Every load this thread issued has landed before the CTA may exit
-            // (immediate when the consumer already waited for it).
-            for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
-                if ((issued_mask >> q) & 1u) {
-                    if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
-                        report_error(p.err, DEV_TIMEOUT_TEARDOWN);
+            // Every load issued has landed before the CTA may exit (immediate
+            // when the consumer already waited for it).
+            if (lane == 0) {
+                for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
+                    if ((issued_mask >> q) & 1u) {
+                        if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
+                            report_error(p.err, DEV_TIMEOUT_TEARDOWN);
+                    }
                 }
             }
         }

@@ -81,7 +81,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
-        if (lane == 0) {
+        // Lanes 0 .. nloads-1 each own one load of every stage and issue them
+        // together; lane 0 waits for the free slot and (even CTA) arms the
+        // stage for both CTAs' bytes.
+        const uint32_t nloads = stage_loads(p);
+        if ((uint32_t)lane < nloads) {
+            const uint32_t lmask = (1u << nloads) - 1u;
+            const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
             uint32_t s = 0, ph = 0;
             uint32_t issued_mask = 0, issued_ph = 0;
             bool skip_one = p.stall != 0;
@@ -89,11 +95,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t t = cluster_id; t < p.total_tiles && ok; t += nclusters) {
                 int b, mb, nb;
                 decode_tile(p, t, b, mb, nb);
-                const int32_t m0 = mb * (2 * kBM) + (int32_t)rank * kBM;   // this CTA's A rows
-                const int32_t n0 = nb * p.BN + (int32_t)rank * half_bn;    // this CTA's B columns
+                // this CTA's A rows / B columns
+                const int32_t mn0 = slot.is_a ? mb * (2 * kBM) + (int32_t)rank * kBM
+                                              : nb * p.BN + (int32_t)rank * half_bn;
                 for (int kb = 0; kb < p.num_k; ++kb) {
-                    if (!mbar_wait(empty_bar(s), ph ^ 1u, budget)) {
-                        report_error(p.err, DEV_TIMEOUT_PRODUCER);
+                    int good = 1;
+                    if (lane == 0) good = mbar_wait(empty_bar(s), ph ^ 1u, budget) ? 1 : 0;
+                    good = __shfl_sync(lmask, good, 0);
+                    if (!good) {
+                        if (lane == 0) report_error(p.err, DEV_TIMEOUT_PRODUCER);
                         ok = false;
                         break;
                     }
@@ -101,36 +111,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         skip_one = false;          // test hook: this stage never fills
                     } else {
                         const uint32_t st = base + s * p.stage_stride;
-                        const int32_t k0 = kb * kBK;
                         const uint32_t fb = mapa_shared(full_bar(s), lead);
-                        if (rank == 0) {
+                        if (rank == 0 && lane == 0) {
                             mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);   // both CTAs' bytes
                             issued_mask |= 1u << s;
                             issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
                         }
-                        if (p.a_fused) {
-                            tma_load_4d_pair(st, &tmA, fb, 0, k0, m0 / 64, b);
-                        } else {
-                            for (uint32_t j = 0; j < p.a_nbox; ++j) {
-                                const uint32_t dst = st + j * p.a_box_bytes;
-                                if (p.a_mn_major) tma_load_3d_pair(dst, &tmA, fb, m0 + 64 * j, k0, b);
-                                else tma_load_3d_pair(dst, &tmA, fb, k0, m0 + p.a_box_mn * j, b);
-                            }
-                        }
-                        if (p.b_fused) {
-                            tma_load_4d_pair(st + p.b_off, &tmB, fb, 0, k0, n0 / 64, b);
-                        } else {
-                            for (uint32_t j = 0; j < p.b_nbox; ++j) {
-                                const uint32_t dst = st + p.b_off + j * p.b_box_bytes;
-                                if (p.b_mn_major) tma_load_3d_pair(dst, &tmB, fb, n0 + 64 * j, k0, b);
-                                else tma_load_3d_pair(dst, &tmB, fb, k0, n0 + p.b_box_mn * j, b);
-                            }
-                        }
+                        __syncwarp(lmask);
+                        int32_t c0, c1, c2;
+                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
+                        tma_load_4d_pair(st + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
                     }
                     if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
                 }
             }
-            if (rank == 0) {
+            if (lane == 0 && rank == 0) {
                 // Every armed stage has received both CTAs' bytes (immediate when
                 // the MMA thread already consumed it).
                 for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
@@ -139,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             report_error(p.err, DEV_TIMEOUT_TEARDOWN);
                     }
                 }
-            } else if (!ok) {
+            } else if (lane == 0 && !ok) {
                 // The odd CTA cannot observe the even CTA's barrier: after a
                 // timeout give its own loads in flight a bounded time to land.
                 const uint64_t t0 = globaltimer();
