@@ -50,9 +50,12 @@ def load_peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the GEMM kernel's sources (the shared-memory probe excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shared_memory_operand_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
+        if name.startswith("smem_probe"):
+            continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

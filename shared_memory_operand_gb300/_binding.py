@@ -25,7 +25,7 @@ DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32}
 
 # Every symbol include/smo_gemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_ex", "gemm_check", "gemm_status_string", "gemm_set_timeout_ns",
-           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc")
+           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "smem_bank_probe")
 
 
 class GemmError(RuntimeError):
@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH, build: bool = False) -> ctypes.CDLL:
     L.gemm_ex_noalloc.restype = i32
     L.gemm_ex_noalloc.argtypes = [vp, i64, i32, vp, i64, i32, vp, i64, i64, i64, i64, i32, i32, i64,
                                   i64, i64, i64, vp]
+    L.smem_bank_probe.restype = i32
+    L.smem_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
     L.gemm_check.restype = i32
     L.gemm_check.argtypes = [vp]
     L.gemm_status_string.restype = ctypes.c_char_p
@@ -164,3 +166,11 @@ def gemm_plan_describe(M, N, K, a_major, b_major, in_dtype="bf16", out_dtype="f3
     L.gemm_plan_describe(M, N, K, a_major, b_major, _dt(in_dtype), _dt(out_dtype), batch, num_sms,
                          buf, n + 1)
     return json.loads(buf.value.decode())
+
+
+def smem_bank_probe(offsets, access_bytes: int, is_store: bool, iters: int, cycles_out, stream=None) -> None:
+    """Times one shared-memory access pattern (see include/smo_probe.h)."""
+    st = load_library().smem_bank_probe(_ptr(offsets), int(access_bytes), 1 if is_store else 0, int(iters),
+                                        _ptr(cycles_out), _stream(stream))
+    if st != 0:
+        raise RuntimeError(f"smem_bank_probe failed: {st}")

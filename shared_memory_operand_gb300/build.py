@@ -20,14 +20,14 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 GENCODE = "arch=compute_103a,code=sm_103a"
 
-SOURCES_CU = ["capi.cu"]
+SOURCES_CU = ["capi.cu", "smem_probe.cu"]
 SOURCES_CPP = ["planner.cpp"]
-HEADERS = ["gemm_kernel.cuh", "ptx.cuh", "gemm_params.h", "planner.h"]
+HEADERS = ["gemm_kernel.cuh", "gemm_kernel_pair.cuh", "gemm_common.cuh", "ptx.cuh", "gemm_params.h", "planner.h"]
 
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in SOURCES_CU + SOURCES_CPP + HEADERS]
-    files.append(os.path.join(INCLUDE, "smo_gemm.h"))
+    files.extend(os.path.join(INCLUDE, h) for h in ("smo_gemm.h", "smo_probe.h"))
     files.append(os.path.abspath(__file__))
     return files
 

@@ -19,7 +19,8 @@ def lib():
 
 
 def _header_functions():
-    text = open(os.path.join(ROOT, "include", "smo_gemm.h")).read()
+    import glob
+    text = "".join(open(f).read() for f in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) - {"if", "defined"})
 
