@@ -54,7 +54,7 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shared_memory_operand_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("smem_probe"):
+        if name.startswith("smem_probe") or name.startswith("tc_probe"):
             continue
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
@@ -271,6 +271,22 @@ def run_ours(args, world, rank, local):
     if st != smo.GEMM_OK:
         raise RuntimeError(smo.gemm_status_string(st))
 
+    # tensor-core issue-rate probe: back-to-back MMAs on resident operands
+    tc_peak = None
+    if rank == 0:
+        probe_out = torch.zeros(2 * 1024, dtype=torch.int64, device=dev)
+        smo.tc_peak_probe(2000, probe_out, 1024, stream=stream)          # warm
+        pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        iters = 20000
+        pe0.record(stream)
+        ncl = smo.tc_peak_probe(iters, probe_out, 1024, stream=stream)
+        pe1.record(stream)
+        torch.cuda.synchronize(dev)
+        tc_flops = ncl * iters * 4 * 2.0 * 256 * 256 * 16
+        tc_peak = {"value": tc_flops / (pe0.elapsed_time(pe1) / 1e3) / 1e12, "unit": "TFLOP/s",
+                   "clusters": ncl, "what": "tcgen05.mma.cta_group::2 256x256x16 bf16 back to back on "
+                                            "resident smem tiles, no loads (smo_probe.h tc_peak_probe)"}
+
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize(dev)
@@ -400,6 +416,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
+        "tensor_peak_probe": tc_peak,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

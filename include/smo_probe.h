@@ -34,6 +34,19 @@ extern "C" {
 int smem_bank_probe(const void* offsets, int access_bytes, int is_store, int iters, void* cycles_out,
                     void* stream);
 
+/*
+ * tc_peak_probe: tensor-core issue-rate probe.  Launches up to max_clusters
+ * 2-CTA clusters (at most one per SM pair) on `stream`; in each, the even CTA
+ * issues iters x 4 back-to-back tcgen05.mma.cta_group::2.kind::f16 of
+ * 256 x 256 x 16 (bf16 in, fp32 accumulate in tensor memory) on operand tiles
+ * resident in shared memory -- no global-memory traffic -- and waits (bounded)
+ * for the last one.  out: device pointer to 2 * max_clusters int64, per
+ * cluster [clock64 cycles, global-timer ns] of its issue loop (-1 on timeout).
+ * Each cluster performs iters * 4 * 2 * 256 * 256 * 16 flops.  Returns the
+ * number of clusters launched, or a negative value on error.  Asynchronous.
+ */
+int tc_peak_probe(int iters, void* out, int max_clusters, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

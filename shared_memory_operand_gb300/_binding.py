@@ -25,7 +25,7 @@ DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32}
 
 # Every symbol include/smo_gemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_ex", "gemm_check", "gemm_status_string", "gemm_set_timeout_ns",
-           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "smem_bank_probe")
+           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "smem_bank_probe", "tc_peak_probe")
 
 
 class GemmError(RuntimeError):
@@ -60,6 +60,8 @@ def load_library(path: str = LIB_PATH, build: bool = False) -> ctypes.CDLL:
                                   i64, i64, i64, vp]
     L.smem_bank_probe.restype = i32
     L.smem_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
+    L.tc_peak_probe.restype = i32
+    L.tc_peak_probe.argtypes = [i32, vp, i32, vp]
     L.gemm_check.restype = i32
     L.gemm_check.argtypes = [vp]
     L.gemm_status_string.restype = ctypes.c_char_p
@@ -174,3 +176,11 @@ def smem_bank_probe(offsets, access_bytes: int, is_store: bool, iters: int, cycl
                                         _ptr(cycles_out), _stream(stream))
     if st != 0:
         raise RuntimeError(f"smem_bank_probe failed: {st}")
+
+
+def tc_peak_probe(iters: int, out, max_clusters: int = 1 << 20, stream=None) -> int:
+    """Tensor-core issue-rate probe (see include/smo_probe.h); returns clusters."""
+    n = load_library().tc_peak_probe(int(iters), _ptr(out), int(max_clusters), _stream(stream))
+    if n < 1:
+        raise RuntimeError(f"tc_peak_probe failed: {n}")
+    return int(n)

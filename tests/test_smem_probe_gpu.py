@@ -65,3 +65,25 @@ def test_page_padding_ordering(measured):
     PAD 1 / 2 / 4 all near the floor ("LDS Optimization", "Padding Amount")."""
     cyc = {p: measured[(f"ld2_pad{p}", False)][1] for p in (0, 1, 2, 4, 32)}
     assert cyc[0] > cyc[32] > 2 * max(cyc[1], cyc[2], cyc[4])
+
+
+def test_tensor_peak_probe_runs_on_every_cluster():
+    """Back-to-back tcgen05.mma.cta_group::2 on resident shared-memory tiles:
+    every cluster finishes within its bounded wait, and the rate is that of a
+    working tensor pipe (a loose floor; the value itself is reported by the
+    bench)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    smo.load_library(build=True)
+    iters = 4000
+    out = torch.full((2 * 1024,), -2, dtype=torch.int64, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    n = smo.tc_peak_probe(iters, out, 1024)
+    e1.record()
+    torch.cuda.synchronize()
+    per = out[: 2 * n].view(n, 2).cpu()
+    assert n >= 1 and torch.all(per[:, 0] > 0) and torch.all(per[:, 1] > 0)
+    flops = n * iters * 4 * 2.0 * 256 * 256 * 16
+    tflops = flops / (e0.elapsed_time(e1) / 1e3) / 1e12
+    assert tflops > 300.0, tflops
