@@ -36,6 +36,15 @@ struct DevState {
     bool attr_set[3] = {false, false, false};
     bool pair_attr_set[3] = {false, false, false};
     int pair_max_clusters[3] = {0, 0, 0};   // co-resident 2-CTA clusters of the pair kernel
+    // Stream-K workspace, one per stream so that GEMMs running concurrently
+    // on different streams never share partial slots or tile counters.
+    struct SkWork {
+        float* work = nullptr;               // partial-accumulator slots (grown on demand)
+        size_t work_bytes = 0;
+        int32_t* flags = nullptr;            // per stream-K tile counters
+        size_t flags_count = 0;
+    };
+    std::map<cudaStream_t, SkWork> sk;
 };
 
 std::mutex g_mu;
@@ -51,6 +60,14 @@ CUtensorMapDataType tmap_type(int dt) {
     return dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
          : dt == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+// Stream-K policy: SMO_GEMM_STREAM_K=0 turns it off, =1 uses it whenever the
+// tile count leaves a partial wave, unset = automatic (see launch_pair).
+int stream_k_mode() {
+    const char* s = std::getenv("SMO_GEMM_STREAM_K");
+    if (!s) return 2;
+    return s[0] == '0' ? 0 : 1;
 }
 
 int force_bn_from_env() {
@@ -190,10 +207,12 @@ int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUt
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM; the persistent grid is
-// as many clusters as can be co-resident (at most one per tile).
+// as many clusters as can be co-resident.  With stream-K the whole tiles are
+// dealt round-robin and the K blocks of the last, partial wave's tiles are
+// shared out evenly, so that every cluster ends at the same time.
 template <int OUT>
-int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
-                const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
+int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                KParams kp, cudaStream_t stream, int stream_k) {
     auto kern = smo::smo_gemm_pair_kernel<OUT>;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
@@ -222,7 +241,69 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
         ds.pair_max_clusters[OUT] = n;
         ds.pair_attr_set[OUT] = true;
     }
-    const int64_t clusters = std::min<int64_t>(pl.tiles, ds.pair_max_clusters[OUT]);
+    const int64_t maxc = ds.pair_max_clusters[OUT];
+    int64_t clusters = std::min<int64_t>(pl.tiles, maxc);
+    kp.sk_clusters = 0;
+    kp.dp_tiles = pl.tiles;
+    kp.sk_units = 0;
+    if (stream_k != 0) {
+        const int64_t waves = pl.tiles / maxc;
+        const int64_t sk_tiles = pl.tiles - waves * maxc;
+        // Each split piece moves a 256 KiB fp32 partial through L2 (about
+        // 20 MB per launch for 76 clusters); measured on GB300 that costs more
+        // than the idle tail it removes unless every cluster's share of the
+        // split tiles is long.  Automatic: at least 48 K blocks per cluster.
+        const bool worth = stream_k == 1 || (sk_tiles * (int64_t)pl.num_k) / maxc >= 48;
+        // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
+        if (worth && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
+            const size_t work_bytes = (size_t)maxc * 2 * smo::kBM * (size_t)pl.BN * sizeof(float);
+            DevState::SkWork* w = nullptr;
+            {
+                std::lock_guard<std::mutex> lk(g_mu);
+                w = &ds.sk[stream];
+            }
+            // No allocation inside a stream capture: a capturing stream without
+            // a large enough workspace yet runs this GEMM without stream-K.
+            cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+                cudaGetLastError();
+                cap = cudaStreamCaptureStatusActive;
+            }
+            const bool can_alloc = cap == cudaStreamCaptureStatusNone;
+            if ((w->work_bytes < work_bytes || w->flags_count < (size_t)maxc) && !can_alloc) goto no_stream_k;
+            if (w->work_bytes < work_bytes) {
+                if (w->work) cudaFree(w->work);
+                w->work = nullptr;
+                w->work_bytes = 0;
+                if (cudaMalloc(&w->work, work_bytes) != cudaSuccess) {
+                    cudaGetLastError();
+                    return GEMM_ERR_LAUNCH;
+                }
+                w->work_bytes = work_bytes;
+            }
+            if (w->flags_count < (size_t)maxc) {
+                if (w->flags) cudaFree(w->flags);
+                w->flags = nullptr;
+                w->flags_count = 0;
+                if (cudaMalloc(&w->flags, sizeof(int32_t) * (size_t)maxc) != cudaSuccess) {
+                    cudaGetLastError();
+                    return GEMM_ERR_LAUNCH;
+                }
+                w->flags_count = (size_t)maxc;
+            }
+            if (cudaMemsetAsync(w->flags, 0, sizeof(int32_t) * (size_t)sk_tiles, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+            clusters = maxc;
+            kp.sk_clusters = (int32_t)maxc;
+            kp.dp_tiles = waves * maxc;
+            kp.sk_units = sk_tiles * (int64_t)pl.num_k;
+            kp.sk_work = w->work;
+            kp.sk_flags = w->flags;
+        }
+    }
+no_stream_k:
     cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp) != cudaSuccess) {
         cudaGetLastError();
@@ -233,8 +314,8 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
 
 template <int OUT>
 int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-           const KParams& kp, cudaStream_t stream) {
-    return pl.pair ? launch_pair<OUT>(pl, ds, ta, tb, tc, kp, stream)
+           const KParams& kp, cudaStream_t stream, int stream_k) {
+    return pl.pair ? launch_pair<OUT>(pl, ds, ta, tb, tc, kp, stream, stream_k)
                    : launch_single<OUT>(pl, ds, ta, tb, tc, kp, stream);
 }
 
@@ -322,9 +403,10 @@ int check_args(const void* A, int64_t lda, int a_major, const void* B, int64_t l
 
 // Plans, encodes the tensor maps and launches, for already-checked arguments
 // on a device whose state `ds` is ready; `err` is the kernel's error word.
-int run_gemm(DevState& ds, int32_t* err, const void* A, int64_t lda, int a_major, const void* B, int64_t ldb,
-             int b_major, void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int in_dtype, int out_dtype,
-             int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC, cudaStream_t stream) {
+int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t lda, int a_major,
+             const void* B, int64_t ldb, int b_major, void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+             int in_dtype, int out_dtype, int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
+             cudaStream_t stream) {
     const int64_t oes = elem_size(out_dtype);
     if (K == 0) {
         for (int64_t b = 0; b < batch; ++b) {
@@ -376,9 +458,9 @@ int run_gemm(DevState& ds, int32_t* err, const void* A, int64_t lda, int a_major
     kp.stall = g_stall.load();
 
     switch (out_dtype) {
-        case GEMM_F32: return launch<smo::OUT_F32>(*pl, ds, ta, tb, tc, kp, stream);
-        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, ds, ta, tb, tc, kp, stream);
-        default: return launch<smo::OUT_F16>(*pl, ds, ta, tb, tc, kp, stream);
+        case GEMM_F32: return launch<smo::OUT_F32>(*pl, ds, ta, tb, tc, kp, stream, stream_k);
+        case GEMM_BF16: return launch<smo::OUT_BF16>(*pl, ds, ta, tb, tc, kp, stream, stream_k);
+        default: return launch<smo::OUT_F16>(*pl, ds, ta, tb, tc, kp, stream, stream_k);
     }
 }
 
@@ -396,8 +478,8 @@ int gemm_ex(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb,
     DevState* ds = nullptr;
     st = device_state(&ds);
     if (st != GEMM_OK) return st;
-    return run_gemm(*ds, ds->d_err, A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype, out_dtype, batch,
-                    strideA, strideB, strideC, reinterpret_cast<cudaStream_t>(stream_));
+    return run_gemm(*ds, ds->d_err, stream_k_mode(), A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype,
+                    out_dtype, batch, strideA, strideB, strideC, reinterpret_cast<cudaStream_t>(stream_));
 }
 
 int gemm_bf16(const void* A, int64_t lda, int a_major, const void* B, int64_t ldb, int b_major, void* C,
@@ -482,8 +564,9 @@ int gemm_ex_noalloc(const void* A, int64_t lda, int a_major, const void* B, int6
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    return run_gemm(na->ds, na->scratch, A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype, out_dtype,
-                    batch, strideA, strideB, strideC, stream);
+    // stream-K would need a workspace: this entry point never splits tiles
+    return run_gemm(na->ds, na->scratch, 0, A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype,
+                    out_dtype, batch, strideA, strideB, strideC, stream);
 }
 
 }  // extern "C"

@@ -77,6 +77,90 @@ __device__ __forceinline__ void slot_coords(const LoadSlot& s, int32_t mn0, int3
     }
 }
 
+// ---------------------------------------------------------------- work items
+// One unit of a CTA's (or CTA pair's) work: K blocks [kb0, kb1) of one tile.
+enum WorkRole : int32_t {
+    ROLE_WHOLE = 0,     // every K block: normal epilogue
+    ROLE_OWNER = 1,     // the tile's first K blocks: adds the later pieces' partials, then the epilogue
+    ROLE_PARTIAL = 2,   // later K blocks of a tile: publishes an fp32 partial into this cluster's slot
+};
+
+struct WorkItem {
+    int64_t tile;
+    int32_t kb0, kb1;
+    int32_t role;
+    int32_t sk_tile;    // index among the stream-K tiles (ROLE_OWNER / ROLE_PARTIAL)
+    int32_t last_slot;  // ROLE_OWNER: partials come from clusters (self, last_slot]
+};
+
+struct WorkIter {
+    int64_t dp, dp_stride;      // next whole tile, stride = clusters
+    int64_t u, u1;              // stream-K unit cursor and end
+    int64_t self;               // this cluster
+};
+
+// First stream-K unit of cluster c.
+__device__ __forceinline__ int64_t sk_bound(const KParams& p, int64_t c) {
+    return c * p.sk_units / p.sk_clusters;
+}
+
+// Cluster whose unit range holds unit u: the largest c with sk_bound(c) <= u.
+__device__ __forceinline__ int64_t sk_cluster_of(const KParams& p, int64_t u) {
+    return ((u + 1) * p.sk_clusters + p.sk_units - 1) / p.sk_units - 1;
+}
+
+__device__ __forceinline__ void work_begin(const KParams& p, int64_t cluster, int64_t nclusters, WorkIter& it) {
+    it.dp = cluster;
+    it.dp_stride = nclusters;
+    it.self = cluster;
+    if (p.sk_clusters > 0) {
+        it.u = sk_bound(p, cluster);
+        it.u1 = sk_bound(p, cluster + 1);
+    } else {
+        it.u = it.u1 = 0;
+    }
+}
+
+__device__ __forceinline__ bool work_next(const KParams& p, WorkIter& it, WorkItem& w) {
+    if (it.dp < p.dp_tiles) {
+        w.tile = it.dp;
+        w.kb0 = 0;
+        w.kb1 = p.num_k;
+        w.role = ROLE_WHOLE;
+        w.sk_tile = -1;
+        w.last_slot = -1;
+        it.dp += it.dp_stride;
+        return true;
+    }
+    if (it.u < it.u1) {
+        const int64_t j = it.u / p.num_k;
+        const int32_t kb0 = (int32_t)(it.u - j * p.num_k);
+        const int32_t kb1 = (int32_t)min((int64_t)p.num_k, kb0 + (it.u1 - it.u));
+        w.tile = p.dp_tiles + j;
+        w.kb0 = kb0;
+        w.kb1 = kb1;
+        w.sk_tile = (int32_t)j;
+        w.last_slot = -1;
+        if (kb0 != 0) {
+            w.role = ROLE_PARTIAL;
+        } else if (kb1 == p.num_k) {
+            w.role = ROLE_WHOLE;
+        } else {
+            w.role = ROLE_OWNER;
+            w.last_slot = (int32_t)sk_cluster_of(p, (j + 1) * p.num_k - 1);
+        }
+        it.u += kb1 - kb0;
+        return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* ptr) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 template <int OUT>
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     const float a = __uint_as_float(lo), b = __uint_as_float(hi);
@@ -89,6 +173,51 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     }
 }
 
+// Partial accumulators are stored in the order a warp holds them after
+// tcgen05.ld.32x32b: for 32-column chunk j, column i of lane l (the warp's
+// row l) at [(j * 32 + i) * 32 + l] -- every store and load of a warp is one
+// contiguous 128-byte line.
+
+// acc[i] (fp32 bits) += slot_s[(chunk32 * 32 + i) * 32 + lane] for every slot
+// s set in `mask`, in increasing slot order (a fixed order: the sum does not
+// depend on timing).
+__device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float* parts, int64_t stride,
+                                             uint32_t mask, int chunk32, int lane) {
+    for (uint32_t m = mask; m; m &= m - 1) {
+        const int s = __ffs(m) - 1;
+        const float* src = parts + (int64_t)s * stride + (int64_t)chunk32 * 32 * 32 + lane;
+        float q[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) q[i] = __ldcg(src + i * 32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(__uint_as_float(acc[i]) + q[i]);
+    }
+}
+
+// Stream-K partial piece: this warp's 32 accumulator rows (all BN columns,
+// fp32) go to `dst` in the order above, then the warp announces them on
+// `flag`.  `release` is called once the accumulator has been read.
+template <typename Release>
+__device__ __forceinline__ void epilogue_partial(const KParams& p, uint32_t tmem_acc, uint32_t lane_field, int lane,
+                                                 float* dst, int32_t* flag, Release release) {
+    for (int c = 0; c < p.BN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_acc + lane_field + (uint32_t)(c * 32), v);
+        tmem_ld_wait();
+        if (c == p.BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+        float* out = dst + (int64_t)c * 32 * 32 + lane;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) __stcg(out + i * 32, __uint_as_float(v[i]));
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(flag, 1);
+}
+
 // Epilogue of one accumulator tile for one warp: its 32 rows (TMEM lanes
 // 32*(warp % 4) ...), all p.epi_chunks column chunks of 128 bytes.
 //   tmem_acc : tensor-memory address of the accumulator (lane field 0)
@@ -99,7 +228,9 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
 template <int OUT, typename Release>
 __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
                                               uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
-                                              int32_t m0, int32_t n0, int b, Release release) {
+                                              int32_t m0, int32_t n0, int b, Release release,
+                                              const float* parts = nullptr, int64_t part_stride = 0,
+                                              uint32_t part_mask = 0) {
     constexpr int kOutBytes = (OUT == OUT_F32) ? 4 : 2;
     constexpr int kChunkCols = 128 / kOutBytes;
     for (int c = 0; c < p.epi_chunks; ++c) {
@@ -111,11 +242,16 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
         if (OUT == OUT_F32) {
             tmem_ld_32x32b_x32(tmem_acc + lane_field + col, v);
             tmem_ld_wait();
+            if (parts) add_partials(v, parts, part_stride, part_mask, c, lane);
         } else {
             uint32_t r0[32], r1[32];
             tmem_ld_32x32b_x32(tmem_acc + lane_field + col, r0);
             tmem_ld_32x32b_x32(tmem_acc + lane_field + col + 32, r1);
             tmem_ld_wait();
+            if (parts) {
+                add_partials(r0, parts, part_stride, part_mask, 2 * c, lane);
+                add_partials(r1, parts, part_stride, part_mask, 2 * c + 1, lane);
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 v[i] = pack2<OUT>(r0[2 * i], r0[2 * i + 1]);

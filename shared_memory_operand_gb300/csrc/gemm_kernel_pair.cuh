@@ -92,13 +92,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued_mask = 0, issued_ph = 0;
             bool skip_one = p.stall != 0;
             bool ok = true;
-            for (int64_t t = cluster_id; t < p.total_tiles && ok; t += nclusters) {
+            WorkIter wi;
+            WorkItem w;
+            work_begin(p, cluster_id, nclusters, wi);
+            while (ok && work_next(p, wi, w)) {
                 int b, mb, nb;
-                decode_tile(p, t, b, mb, nb);
+                decode_tile(p, w.tile, b, mb, nb);
                 // this CTA's A rows / B columns
                 const int32_t mn0 = slot.is_a ? mb * (2 * kBM) + (int32_t)rank * kBM
                                               : nb * p.BN + (int32_t)rank * half_bn;
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     int good = 1;
                     if (lane == 0) good = mbar_wait(empty_bar(s), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
@@ -149,7 +152,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t s = 0, ph = 0;
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = cluster_id; t < p.total_tiles && ok; t += nclusters, ++it) {
+            WorkIter wi;
+            WorkItem w;
+            work_begin(p, cluster_id, nclusters, wi);
+            for (; ok && work_next(p, wi, w); ++it) {
                 const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
                 if (!mbar_wait(acce_bar(buf), aph ^ 1u, budget)) {
                     report_error(p.err, DEV_TIMEOUT_MMA);
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(full_bar(s), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < kBK / kMmaK; ++k) {
                         umma_f16_pair(d_tmem, a_desc + (uint64_t)((k * p.a_kstep) >> 4),
-                                      b_desc + (uint64_t)((k * p.b_kstep) >> 4), p.idesc, (kb | k) != 0);
+                                      b_desc + (uint64_t)((k * p.b_kstep) >> 4), p.idesc, (kb - w.kb0) | k);
                     }
                     umma_commit_pair_mc(empty_bar(s), (uint16_t)(3u << lead));   // both CTAs' stage s free
                     if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
@@ -189,9 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = (uint32_t)warp & 3u;
         const uint32_t lane_field = (q * 32u) << 16;
         uint32_t it = 0, sbuf = 0;
-        for (int64_t t = cluster_id; t < p.total_tiles; t += nclusters, ++it) {
+        WorkIter wi;
+        WorkItem w;
+        work_begin(p, cluster_id, nclusters, wi);
+        const int64_t slot_floats = 2 * kBM * (int64_t)p.BN;          // one cluster's partial slot
+        // this warp's region of a slot: 32 rows x BN fp32
+        const int64_t warp_rows = ((int64_t)rank * kEpiWarps + (int64_t)q) * kEpiRowsPerWarp * p.BN;
+        for (; work_next(p, wi, w); ++it) {
             int b, mb, nb;
-            decode_tile(p, t, b, mb, nb);
+            decode_tile(p, w.tile, b, mb, nb);
             const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
             int good = 1;
             if (lane == 0) good = mbar_wait(accf_bar(buf), aph, budget) ? 1 : 0;
@@ -201,11 +213,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
+            const uint32_t acce = mapa_shared(acce_bar(buf), lead);
+            const uint32_t acc = tmem_base + buf * (uint32_t)p.BN;
+            if (w.role == ROLE_PARTIAL) {
+                // later K blocks of a stream-K tile: publish the fp32 partial
+                epilogue_partial(p, acc, lane_field, lane, p.sk_work + cluster_id * slot_floats + warp_rows,
+                                 p.sk_flags + w.sk_tile, [&] { mbar_arrive_cluster(acce); });
+                continue;
+            }
+            uint32_t mask = 0;
+            if (w.role == ROLE_OWNER) {
+                // partials of clusters (self, last_slot] with a non-empty range,
+                // 8 epilogue warps each (4 per CTA of the pair)
+                int32_t want = 0;
+                for (int64_t c = cluster_id + 1; c <= w.last_slot; ++c) {
+                    if (sk_bound(p, c) < sk_bound(p, c + 1)) {
+                        mask |= 1u << (uint32_t)(c - cluster_id - 1);
+                        want += 2 * kEpiWarps;
+                    }
+                }
+                int ready = 1;
+                if (lane == 0) {
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire_gpu(p.sk_flags + w.sk_tile) < want) {
+                        if ((int64_t)(globaltimer() - t0) > budget) {
+                            ready = 0;
+                            break;
+                        }
+                    }
+                }
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (!ready) {
+                    if (lane == 0) report_error(p.err, DEV_TIMEOUT_FIXUP);
+                    mask = 0;
+                } else {
+                    (void)ld_acquire_gpu(p.sk_flags + w.sk_tile);    // every lane acquires
+                }
+            }
             const int32_t m0 = mb * (2 * kBM) + (int32_t)rank * kBM + (int32_t)q * kEpiRowsPerWarp;
             const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
-            const uint32_t acce = mapa_shared(acce_bar(buf), lead);
-            epilogue_tile<OUT>(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane, m0,
-                               nb * p.BN, b, [&] { mbar_arrive_cluster(acce); });
+            epilogue_tile<OUT>(p, &tmC, acc, lane_field, slabs, sbuf, lane, m0, nb * p.BN, b,
+                               [&] { mbar_arrive_cluster(acce); },
+                               mask ? p.sk_work + (cluster_id + 1) * slot_floats + warp_rows : nullptr,
+                               slot_floats, mask);
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();

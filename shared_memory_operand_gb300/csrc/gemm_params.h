@@ -27,6 +27,7 @@ enum DevErr : int32_t {
     DEV_TIMEOUT_MMA = 2,
     DEV_TIMEOUT_EPILOGUE = 3,
     DEV_TIMEOUT_TEARDOWN = 4,
+    DEV_TIMEOUT_FIXUP = 5,
 };
 
 struct KParams {
@@ -53,6 +54,15 @@ struct KParams {
     void* C;                        // output base (ragged 16-byte row tails are stored directly)
     int64_t ldc, strideC;           // elements
     int32_t n_tma;                  // columns [0, n_tma) are written by TMA (n_tma * es % 16 == 0)
+    // Stream-K (CTA-pair kernel): tiles [0, dp_tiles) are computed whole,
+    // round-robin over the clusters; the K blocks of the remaining tiles
+    // (sk_units in all) are shared out evenly, cluster c taking units
+    // [c * sk_units / sk_clusters, (c + 1) * sk_units / sk_clusters).
+    int32_t sk_clusters;            // clusters of the launch; 0 = no stream-K
+    int64_t dp_tiles;
+    int64_t sk_units;
+    float* sk_work;                 // one fp32 partial-accumulator slot per cluster
+    int32_t* sk_flags;              // per stream-K tile: epilogue warps that published
     int32_t* err;                   // device error word
     int64_t timeout_ns;             // budget of each bounded wait
     int32_t stall;                  // test hook: skip the first TMA load

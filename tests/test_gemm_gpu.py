@@ -235,3 +235,54 @@ def test_config_skinny():
 
 def test_config_batched():
     _sampled(workload("batched_32x2048_bf16"), count=4000)
+
+
+# ------------------------------------------------------------ stream-K (CTA pair)
+def _pair_tiles(M, N):
+    return ((M + 255) // 256) * ((N + 255) // 256)
+
+
+@pytest.mark.parametrize("M,N,K,dist", [
+    (2560, 2048, 512, "uniform"),     # 80 tiles: one whole wave + 4 tiles split over all clusters
+    (1024, 1024, 640, "uniform"),     # 16 tiles, fewer than the clusters: every tile split
+    (2560, 2048, 520, "int"),         # K tail inside the split range, integers: bit-exact
+    (1800, 1100, 700, "normal"),      # ragged M, N
+])
+def test_stream_k_tiles_full_compare(M, N, K, dist, monkeypatch):
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
+    p = make_problem(M, N, K, a_major=K_MAJOR, b_major=MN_MAJOR, dist=dist, seed=M + K,
+                     out_dtype="f32" if dist == "int" else "bf16")
+    _full(p, exact=(dist == "int"))
+
+
+def test_stream_k_timeout_reports_and_recovers(monkeypatch):
+    """With tiles split along K, a stalled stage makes the owners' bounded
+    waits for the other pieces run out as well: still one clean error."""
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
+    old = smo.gemm_set_timeout_ns(20_000_000)
+    try:
+        smo.gemm_debug_inject_stall(True)
+        A = torch.zeros(2560, 512, dtype=torch.bfloat16, device="cuda")
+        B = torch.zeros(512, 2048, dtype=torch.bfloat16, device="cuda")
+        C = torch.zeros(2560, 2048, dtype=torch.float32, device="cuda")
+        smo.gemm_ex(A, 512, 0, B, 2048, 1, C, 2048, 2560, 2048, 512, out_dtype="f32")
+        assert smo.gemm_check() == smo.GEMM_ERR_TIMEOUT
+    finally:
+        smo.gemm_debug_inject_stall(False)
+        smo.gemm_set_timeout_ns(old)
+    assert smo.gemm_check() == smo.GEMM_OK
+    p = make_problem(2560, 2048, 512, dist="uniform", seed=3, out_dtype="f32")
+    check(p, run_gpu(p), oracle_full(p))
+
+
+def test_stream_k_is_deterministic_and_matches_whole_tiles(monkeypatch):
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
+    p = make_problem(2560, 2048, 768, dist="uniform", seed=5, out_dtype="f32")
+    first = run_gpu(p)
+    again = run_gpu(p)
+    assert np.array_equal(first, again)                     # fixed-order fix-up
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "0")
+    whole = run_gpu(p)
+    check(p, first, whole.astype(np.float64))               # same product, other split
+    ref = oracle_full(p)
+    check(p, first, ref)
