@@ -258,7 +258,7 @@ def run_ours(args, world, rank, local):
     B = p.B.to(dev)
     odt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[p.out_dtype]
     C = torch.empty(p.c_numel(), dtype=odt, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    stream = torch.cuda.Stream(dev) if args.graph else torch.cuda.current_stream(dev)
 
     def launch(a=A, b=B, c=C):
         smo.gemm_ex(a, p.lda, p.a_major, b, p.ldb, p.b_major, c, p.ldc, p.M, p.N, p.K,
@@ -294,23 +294,56 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
+    # Inputs + output larger than twice the 129 MB L2 stream from HBM anyway;
+    # smaller working sets get L2 flushed (256 MiB written) before every launch,
+    # outside the per-launch event pair.
+    work_bytes = (p.A.numel() + p.B.numel()) * 2 + C.numel() * C.element_size()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if work_bytes < (258 << 20) else None
+    def timing_event():
+        # events recorded inside a CUDA graph need the "external" record flag to be timed
+        if args.graph:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        return torch.cuda.Event(enable_timing=True)
+
+    ev = [(timing_event(), timing_event()) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    graph = None
+    if args.graph:
+        # launch-bound shapes: the K launches (and their event pairs) replayed
+        # from one CUDA graph, so host call overhead is not in the device time
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(args.steps):
+                if flush is not None:
+                    flush.zero_()
+                ev[i][0].record(stream)
+                launch()
+                ev[i][1].record(stream)
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
     t_start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        launch()
-        ev[i][1].record(stream)
+    if graph is not None:
+        with torch.cuda.stream(stream):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            ev[i][0].record(stream)
+            launch()
+            ev[i][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
-    total_s = t_start.elapsed_time(t_end) / 1e3
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    # with L2 flushes between launches a step is the launch itself (sum of the
+    # launch event pairs); otherwise the whole timed region
+    total_s = (sum(launch_ms) if flush is not None else t_start.elapsed_time(t_end)) / 1e3
     st = smo.gemm_check(stream)
     if st != smo.GEMM_OK:
         raise RuntimeError(smo.gemm_status_string(st))
@@ -410,7 +443,10 @@ def run_ours(args, world, rank, local):
                    "a_major": "M" if p.a_major else "K", "b_major": "N" if p.b_major else "K",
                    "in": p.in_dtype, "accumulate": "f32", "out": p.out_dtype,
                    "dist": p.dist, "seed": p.seed, "parallelism": f"replicas{world}",
-                   "l2": "no flush: A+B+C resident set larger than L2 (129 MB)",
+                   "l2": ("flushed before every launch (256 MiB memset between the launch event "
+                          "pairs; steps timed by those pairs)") if flush is not None else
+                         "no flush: A+B+C larger than twice the 129 MB L2",
+                   "launch": "cuda graph replay" if args.graph else "back-to-back host launches",
                    "pct_of_dense_bf16_peak": 100.0 * agg["value"] / world / peak},
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -437,6 +473,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-check", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the timed launches from a CUDA graph (launch-bound shapes)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
