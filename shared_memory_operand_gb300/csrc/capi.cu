@@ -70,6 +70,15 @@ int stream_k_mode() {
     return s[0] == '0' ? 0 : 1;
 }
 
+// Measurement knob: stages per barrier pair (1 or 2) instead of the planner's.
+int kgroup_from_env(int planned, int stages) {
+    const char* s = std::getenv("SMO_GEMM_KGROUP");
+    if (!s) return planned;
+    int v = std::atoi(s);
+    if (v == 2 && stages >= 4) return 2;
+    return v == 1 ? 1 : planned;
+}
+
 int force_bn_from_env() {
     const char* s = std::getenv("SMO_GEMM_FORCE_BN");
     if (!s) return 0;
@@ -456,6 +465,7 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     kp.err = err;
     kp.timeout_ns = g_timeout_ns.load();
     kp.stall = g_stall.load();
+    kp.kgroup = kgroup_from_env(kp.kgroup, kp.stages);
 
     switch (out_dtype) {
         case GEMM_F32: return launch<smo::OUT_F32>(*pl, ds, ta, tb, tc, kp, stream, stream_k);

@@ -2,10 +2,11 @@
 //
 //   warp 0 (one thread)  TMA producer: fills a ring of `stages` shared-memory
 //                        stages with 128-byte-swizzled A and B tiles
-//                        (cp.async.bulk.tensor, mbarrier complete_tx).
+//                        (cp.async.bulk.tensor, mbarrier complete_tx), handed
+//                        over in groups of `kgroup` stages per barrier pair.
 //   warp 1 (one thread)  MMA issuer: 4 x tcgen05.mma (128 x BN x 16) per stage,
 //                        accumulating in tensor memory; tcgen05.commit frees
-//                        the stage (split barrier) and, after the last K block,
+//                        the group (split barrier) and, after the last K block,
 //                        publishes the accumulator.
 //   warps 2..5           epilogue: tcgen05.ld -> fp32/bf16/f16 -> conflict-free
 //                        swizzled st.shared -> TMA store (clips ragged edges).
@@ -35,6 +36,8 @@
 #include "gemm_common.cuh"
 
 namespace smo {
+
+static_assert(kBK / kMmaK == 4, "the issue loops unroll four MMAs per K block");
 
 template <int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -89,17 +92,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((uint32_t)lane < nloads) {
             const uint32_t lmask = (1u << nloads) - 1u;
             const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
-            uint32_t s = 0, ph = 0;
-            uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per stage (lane 0)
+            const int kg = p.kgroup;
+            const uint32_t ngroups = (uint32_t)(p.stages / kg);
+            uint32_t g = 0, ph = 0;
+            uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per group (lane 0)
             bool skip_one = p.stall != 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
                 int b, mb, nb;
                 decode_tile(p, t, b, mb, nb);
                 const int32_t mn0 = slot.is_a ? mb * kBM : nb * p.BN;
-                for (int kb = 0; kb < p.num_k; ++kb) {
+                for (int kb = 0; kb < p.num_k; kb += kg) {
+                    const int n = min(kg, p.num_k - kb);        // K blocks in this group
                     int good = 1;
-                    if (lane == 0) good = mbar_wait(empty_bar(s), ph ^ 1u, budget) ? 1 : 0;
+                    if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
                     if (!good) {
                         if (lane == 0) report_error(p.err, DEV_TIMEOUT_PRODUCER);
@@ -107,26 +113,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (skip_one) {
-                        skip_one = false;          // test hook: this stage never fills
+                        skip_one = false;          // test hook: this group never fills
                     } else {
-                        const uint32_t st = base + s * p.stage_stride;
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);
-                            issued_mask |= 1u << s;
-                            issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                            mbar_arrive_expect_tx(full_bar(g), (uint32_t)n * p.tx_bytes);
+                            issued_mask |= 1u << g;
+                            issued_ph = (issued_ph & ~(1u << g)) | (ph << g);
                         }
                         __syncwarp(lmask);
-                        int32_t c0, c1, c2;
-                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
-                        tma_load_4d(st + slot.dst_off, slot.tm, full_bar(s), c0, c1, c2, b);
+                        for (int j = 0; j < n; ++j) {
+                            const uint32_t st = base + (g * (uint32_t)kg + (uint32_t)j) * p.stage_stride;
+                            int32_t c0, c1, c2;
+                            slot_coords(slot, mn0, (kb + j) * kBK, c0, c1, c2);
+                            tma_load_4d(st + slot.dst_off, slot.tm, full_bar(g), c0, c1, c2, b);
+                        }
                     }
-                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                    if (++g == ngroups) { g = 0; ph ^= 1u; }
                 }
             }
             // Every load issued has landed before the CTA may exit (immediate
             // when the consumer already waited for it).
             if (lane == 0) {
-                for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
+                for (uint32_t q = 0; q < (uint32_t)(p.stages / p.kgroup); ++q) {
                     if ((issued_mask >> q) & 1u) {
                         if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
                             report_error(p.err, DEV_TIMEOUT_TEARDOWN);
@@ -138,7 +146,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t s = 0, ph = 0;
+            // Descriptors, steps and ring bounds sit in registers: one thread
+            // issues every MMA, and its per-K-block instruction latency must
+            // stay below the tensor pipe's time for that block.
+            const int kg = p.kgroup;
+            const uint32_t ngroups = (uint32_t)(p.stages / kg);
+            const uint32_t desc_step = p.stage_stride >> 4;
+            const uint64_t a_desc0 = p.a_desc_hi | (uint64_t)((base >> 4) & 0x3FFFu);
+            const uint64_t b_desc0 = p.b_desc_hi | (uint64_t)(((base + p.b_off) >> 4) & 0x3FFFu);
+            const uint64_t ak = p.a_kstep >> 4, bk = p.b_kstep >> 4;
+            const uint32_t idesc = p.idesc;
+            uint32_t g = 0, ph = 0;
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
@@ -150,24 +168,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = 0; kb < p.num_k; ++kb) {
-                    if (!mbar_wait(full_bar(s), ph, budget)) {
+                for (int kb = 0; kb < p.num_k; kb += kg) {
+                    const int n = min(kg, p.num_k - kb);
+                    if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = base + s * p.stage_stride;
-                    const uint32_t b_addr = a_addr + p.b_off;
-                    const uint64_t a_desc = p.a_desc_hi | (uint64_t)((a_addr >> 4) & 0x3FFFu);
-                    const uint64_t b_desc = p.b_desc_hi | (uint64_t)((b_addr >> 4) & 0x3FFFu);
-#pragma unroll
-                    for (int k = 0; k < kBK / kMmaK; ++k) {
-                        umma_f16(d_tmem, a_desc + (uint64_t)((k * p.a_kstep) >> 4),
-                                 b_desc + (uint64_t)((k * p.b_kstep) >> 4), p.idesc, (kb | k) != 0);
+                    for (int j = 0; j < n; ++j) {
+                        const uint64_t so = (uint64_t)((g * (uint32_t)kg + (uint32_t)j) * desc_step);
+                        const uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
+                        umma_f16(d_tmem, ad, bd, idesc, (uint32_t)(kb + j != 0));
+                        umma_f16(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                        umma_f16(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                        umma_f16(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     }
-                    umma_commit(empty_bar(s));     // stage free once these MMAs retire
-                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                    umma_commit(empty_bar(g));     // group free once these MMAs retire
+                    if (++g == ngroups) { g = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit(accf_bar(buf));        // accumulator ready for the epilogue

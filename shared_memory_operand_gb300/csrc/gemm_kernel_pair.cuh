@@ -11,11 +11,17 @@
 // output tiles raise arithmetic intensity; Level 9: a cluster of workgroups
 // shares operand panels instead of re-requesting them).
 //
+// The ring's stages are handed over in groups of `kgroup` (two for the
+// 6-stage ring): one full/empty barrier pair, one wait and one commit per
+// group of 2 x 4 MMAs.  A single thread issues every MMA, and with a wait and
+// a commit per 4 MMAs its instruction latency, not the tensor pipe, set the
+// pace.
+//
 // Synchronisation across the pair:
-//   full[s]    (even CTA only) -- both CTAs' TMA loads complete on it
-//                                 (cp.async.bulk.tensor ... .cta_group::2);
+//   full[g]    (even CTA only) -- both CTAs' TMA loads of the group complete
+//                                 on it (cp.async.bulk.tensor ... .cta_group::2);
 //                                 the even producer arms it for both CTAs' bytes
-//   empty[s]   (both)          -- the MMA thread's commit multicasts to both
+//   empty[g]   (both)          -- the MMA thread's commit multicasts to both
 //   acc_full   (both)          -- likewise, after the last K block of a tile
 //   acc_empty  (even CTA only) -- 4 epilogue warps of each CTA arrive
 // Every wait is bounded; cluster barriers at start (barriers initialised,
@@ -28,6 +34,8 @@
 #include "gemm_common.cuh"
 
 namespace smo {
+
+static_assert(kBK / kMmaK == 4, "the issue loop unrolls four MMAs per K block");
 
 template <int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -88,7 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((uint32_t)lane < nloads) {
             const uint32_t lmask = (1u << nloads) - 1u;
             const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
-            uint32_t s = 0, ph = 0;
+            const int kg = p.kgroup;
+            const uint32_t ngroups = (uint32_t)(p.stages / kg);
+            uint32_t g = 0, ph = 0;
             uint32_t issued_mask = 0, issued_ph = 0;
             bool skip_one = p.stall != 0;
             bool ok = true;
@@ -101,9 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this CTA's A rows / B columns
                 const int32_t mn0 = slot.is_a ? mb * (2 * kBM) + (int32_t)rank * kBM
                                               : nb * p.BN + (int32_t)rank * half_bn;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                for (int kb = w.kb0; kb < w.kb1; kb += kg) {
+                    const int n = min(kg, w.kb1 - kb);          // K blocks in this group
                     int good = 1;
-                    if (lane == 0) good = mbar_wait(empty_bar(s), ph ^ 1u, budget) ? 1 : 0;
+                    if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
                     if (!good) {
                         if (lane == 0) report_error(p.err, DEV_TIMEOUT_PRODUCER);
@@ -111,27 +122,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (skip_one) {
-                        skip_one = false;          // test hook: this stage never fills
+                        skip_one = false;          // test hook: this group never fills
                     } else {
-                        const uint32_t st = base + s * p.stage_stride;
-                        const uint32_t fb = mapa_shared(full_bar(s), lead);
+                        const uint32_t fb = mapa_shared(full_bar(g), lead);
                         if (rank == 0 && lane == 0) {
-                            mbar_arrive_expect_tx(full_bar(s), p.tx_bytes);   // both CTAs' bytes
-                            issued_mask |= 1u << s;
-                            issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                            mbar_arrive_expect_tx(full_bar(g), (uint32_t)n * p.tx_bytes);   // both CTAs' bytes
+                            issued_mask |= 1u << g;
+                            issued_ph = (issued_ph & ~(1u << g)) | (ph << g);
                         }
                         __syncwarp(lmask);
-                        int32_t c0, c1, c2;
-                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
-                        tma_load_4d_pair(st + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
+                        for (int j = 0; j < n; ++j) {
+                            const uint32_t st = base + (g * (uint32_t)kg + (uint32_t)j) * p.stage_stride;
+                            int32_t c0, c1, c2;
+                            slot_coords(slot, mn0, (kb + j) * kBK, c0, c1, c2);
+                            tma_load_4d_pair(st + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
+                        }
                     }
-                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                    if (++g == ngroups) { g = 0; ph ^= 1u; }
                 }
             }
             if (lane == 0 && rank == 0) {
-                // Every armed stage has received both CTAs' bytes (immediate when
+                // Every armed group has received both CTAs' bytes (immediate when
                 // the MMA thread already consumed it).
-                for (uint32_t q = 0; q < (uint32_t)p.stages; ++q) {
+                for (uint32_t q = 0; q < (uint32_t)(p.stages / p.kgroup); ++q) {
                     if ((issued_mask >> q) & 1u) {
                         if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
                             report_error(p.err, DEV_TIMEOUT_TEARDOWN);
@@ -149,7 +162,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && rank == 0) {
-            uint32_t s = 0, ph = 0;
+            // Everything the issue loop needs sits in registers: the single
+            // issuing thread, not the tensor pipe, is the limit when each K
+            // block's MMAs wait behind parameter loads and address arithmetic.
+            const int kg = p.kgroup;
+            const uint32_t ngroups = (uint32_t)(p.stages / kg);
+            const uint32_t desc_step = p.stage_stride >> 4;                 // descriptor units per stage
+            const uint64_t a_desc0 = p.a_desc_hi | (uint64_t)((base >> 4) & 0x3FFFu);
+            const uint64_t b_desc0 = p.b_desc_hi | (uint64_t)(((base + p.b_off) >> 4) & 0x3FFFu);
+            const uint64_t ak = p.a_kstep >> 4, bk = p.b_kstep >> 4;
+            const uint32_t idesc = p.idesc;
+            uint32_t g = 0, ph = 0;
             uint32_t it = 0;
             bool ok = true;
             WorkIter wi;
@@ -164,24 +187,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(full_bar(s), ph, budget)) {
+                for (int kb = w.kb0; kb < w.kb1; kb += kg) {
+                    const int n = min(kg, w.kb1 - kb);
+                    if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = base + s * p.stage_stride;
-                    const uint32_t b_addr = a_addr + p.b_off;
-                    const uint64_t a_desc = p.a_desc_hi | (uint64_t)((a_addr >> 4) & 0x3FFFu);
-                    const uint64_t b_desc = p.b_desc_hi | (uint64_t)((b_addr >> 4) & 0x3FFFu);
-#pragma unroll
-                    for (int k = 0; k < kBK / kMmaK; ++k) {
-                        umma_f16_pair(d_tmem, a_desc + (uint64_t)((k * p.a_kstep) >> 4),
-                                      b_desc + (uint64_t)((k * p.b_kstep) >> 4), p.idesc, (kb - w.kb0) | k);
+                    for (int j = 0; j < n; ++j) {
+                        const uint64_t so = (uint64_t)((g * (uint32_t)kg + (uint32_t)j) * desc_step);
+                        const uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
+                        umma_f16_pair(d_tmem, ad, bd, idesc, (uint32_t)(kb + j != w.kb0));
+                        umma_f16_pair(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                        umma_f16_pair(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                        umma_f16_pair(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     }
-                    umma_commit_pair_mc(empty_bar(s), (uint16_t)(3u << lead));   // both CTAs' stage s free
-                    if (++s == (uint32_t)p.stages) { s = 0; ph ^= 1u; }
+                    umma_commit_pair_mc(empty_bar(g), (uint16_t)(3u << lead));   // both CTAs' group g free
+                    if (++g == ngroups) { g = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit_pair_mc(accf_bar(buf), (uint16_t)(3u << lead));       // both accumulators ready

@@ -36,6 +36,7 @@ struct KParams {
     int32_t group_m;
     int64_t tiles_per_batch, total_tiles;
     int32_t BN, stages;
+    int32_t kgroup;                 // K blocks (stages) per full/empty barrier pair: 1 or 2
     uint32_t idesc;                 // tcgen05 instruction descriptor
     uint32_t a_mn_major, b_mn_major;
     uint32_t a_nbox, b_nbox;        // TMA boxes per stage and operand

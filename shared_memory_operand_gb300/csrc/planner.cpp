@@ -227,6 +227,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
         return p;
     }
     p.stages = stages;
+    // Two stages per barrier pair halve the waits and commits the single
+    // MMA-issuing thread executes per MMA.  With fewer than six stages the
+    // ring would have too few groups in flight to hide the load latency.
+    p.kgroup = stages >= 6 ? 2 : 1;
     p.off_epi = stages * p.stage_stride;
     p.off_bar = p.off_epi + epi_bytes;
     p.smem_bytes = p.off_bar + kBarrierBytes + 1024;
@@ -250,6 +254,7 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->tiles_per_batch = (int64_t)p.num_m * p.num_n;
     kp->total_tiles = p.tiles;
     kp->BN = p.BN; kp->stages = p.stages;
+    kp->kgroup = p.kgroup;
     kp->idesc = p.idesc;
     kp->a_mn_major = p.a.mn_major; kp->b_mn_major = p.b.mn_major;
     kp->a_nbox = p.a.nbox; kp->b_nbox = p.b.nbox;
@@ -287,7 +292,7 @@ std::string describe_json(const Plan& p) {
     o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
       << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
       << ",\"pair\":" << p.pair << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << kBK << ",\"mma_k\":" << kMmaK
-      << ",\"stages\":" << p.stages << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
+      << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
       << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads
       << ",\"idesc\":" << p.idesc << ",\"smem_bytes\":" << p.smem_bytes

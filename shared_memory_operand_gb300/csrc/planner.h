@@ -47,6 +47,7 @@ struct Plan {
     int pair = 0;                   // 1: CTA pair (cta_group::2), 256 x BN tiles over two SMs
     int tile_m = 128;               // output rows per tile (128, or 256 for a pair)
     int BN = 256, stages = 4;
+    int kgroup = 1;                 // stages per full/empty barrier pair
     int num_m = 0, num_n = 0, num_k = 0, group_m = 16;
     int64_t tiles = 0;
     int grid = 0, num_sms = 0;
