@@ -33,7 +33,7 @@ struct DevState {
     bool usable = false;
     int num_sms = 0;
     int32_t* d_err = nullptr;
-    bool attr_set[3] = {false, false, false};
+    bool attr_set[6] = {false, false, false, false, false, false};   // [OUT * 2 + KG - 1]
     bool pair_attr_set[3] = {false, false, false};
     int pair_max_clusters[3] = {0, 0, 0};   // co-resident 2-CTA clusters of the pair kernel
     // Stream-K workspace, one per stream so that GEMMs running concurrently
@@ -70,13 +70,22 @@ int stream_k_mode() {
     return s[0] == '0' ? 0 : 1;
 }
 
-// Measurement knob: stages per barrier pair (1 or 2) instead of the planner's.
-int kgroup_from_env(int planned, int stages) {
+// Measurement knob for the one-CTA kernel: stages per barrier pair (1 or 2)
+// instead of the planner's.  The CTA-pair kernel always hands over two.
+int kgroup_from_env(int planned, int stages, int pair) {
     const char* s = std::getenv("SMO_GEMM_KGROUP");
-    if (!s) return planned;
+    if (!s || pair) return planned;
     int v = std::atoi(s);
     if (v == 2 && stages >= 4) return 2;
     return v == 1 ? 1 : planned;
+}
+
+// Measurement knob: M tiles per raster group instead of the planner's.
+int group_m_from_env(int planned, int num_m) {
+    const char* s = std::getenv("SMO_GEMM_GROUP_M");
+    if (!s) return planned;
+    const int v = std::atoi(s);
+    return v >= 1 ? std::min(v, num_m) : planned;
 }
 
 int force_bn_from_env() {
@@ -198,21 +207,28 @@ int encode_fused(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t 
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
 }
 
-template <int OUT>
-int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
-                  const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
-    auto kern = smo::smo_gemm_kernel<OUT>;
-    if (!ds.attr_set[OUT]) {
+template <int OUT, int KG>
+int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
+                     const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
+    auto kern = smo::smo_gemm_kernel<OUT, KG>;
+    if (!ds.attr_set[OUT * 2 + KG - 1]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
             cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
-        ds.attr_set[OUT] = true;
+        ds.attr_set[OUT * 2 + KG - 1] = true;
     }
     kern<<<pl.grid, smo::kThreads, pl.smem_bytes, stream>>>(ta, tb, tc, kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
+}
+
+template <int OUT>
+int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
+                  const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
+    return kp.kgroup == 2 ? launch_single_kg<OUT, 2>(pl, ds, ta, tb, tc, kp, stream)
+                          : launch_single_kg<OUT, 1>(pl, ds, ta, tb, tc, kp, stream);
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM; the persistent grid is
@@ -465,7 +481,8 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     kp.err = err;
     kp.timeout_ns = g_timeout_ns.load();
     kp.stall = g_stall.load();
-    kp.kgroup = kgroup_from_env(kp.kgroup, kp.stages);
+    kp.kgroup = kgroup_from_env(kp.kgroup, kp.stages, pl->pair);
+    kp.group_m = group_m_from_env(kp.group_m, kp.num_m);
 
     switch (out_dtype) {
         case GEMM_F32: return launch<smo::OUT_F32>(*pl, ds, ta, tb, tc, kp, stream, stream_k);

@@ -39,7 +39,8 @@ namespace smo {
 
 static_assert(kBK / kMmaK == 4, "the issue loops unroll four MMAs per K block");
 
-template <int OUT>
+// KG: stages per full/empty barrier pair (1 or 2).
+template <int OUT, int KG>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
@@ -92,9 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((uint32_t)lane < nloads) {
             const uint32_t lmask = (1u << nloads) - 1u;
             const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
-            const int kg = p.kgroup;
-            const uint32_t ngroups = (uint32_t)(p.stages / kg);
-            uint32_t g = 0, ph = 0;
+            const uint32_t ngroups = (uint32_t)(p.stages / KG);
+            const uint32_t group_bytes = KG * p.stage_stride;
+            uint32_t g = 0, ph = 0, gst = base;        // group index, ring parity, group's smem
             uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per group (lane 0)
             bool skip_one = p.stall != 0;
             bool ok = true;
@@ -102,8 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int b, mb, nb;
                 decode_tile(p, t, b, mb, nb);
                 const int32_t mn0 = slot.is_a ? mb * kBM : nb * p.BN;
-                for (int kb = 0; kb < p.num_k; kb += kg) {
-                    const int n = min(kg, p.num_k - kb);        // K blocks in this group
+                for (int kb = 0; kb < p.num_k; kb += KG) {
+                    const bool two = KG == 2 && kb + 1 < p.num_k;   // the last group may hold one block
                     int good = 1;
                     if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
@@ -116,25 +117,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                         skip_one = false;          // test hook: this group never fills
                     } else {
                         if (lane == 0) {
-                            mbar_arrive_expect_tx(full_bar(g), (uint32_t)n * p.tx_bytes);
+                            mbar_arrive_expect_tx(full_bar(g), two ? 2 * p.tx_bytes : p.tx_bytes);
                             issued_mask |= 1u << g;
                             issued_ph = (issued_ph & ~(1u << g)) | (ph << g);
                         }
                         __syncwarp(lmask);
-                        for (int j = 0; j < n; ++j) {
-                            const uint32_t st = base + (g * (uint32_t)kg + (uint32_t)j) * p.stage_stride;
-                            int32_t c0, c1, c2;
-                            slot_coords(slot, mn0, (kb + j) * kBK, c0, c1, c2);
-                            tma_load_4d(st + slot.dst_off, slot.tm, full_bar(g), c0, c1, c2, b);
+                        int32_t c0, c1, c2;
+                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
+                        tma_load_4d(gst + slot.dst_off, slot.tm, full_bar(g), c0, c1, c2, b);
+                        if (two) {
+                            slot_coords(slot, mn0, (kb + 1) * kBK, c0, c1, c2);
+                            tma_load_4d(gst + p.stage_stride + slot.dst_off, slot.tm, full_bar(g), c0, c1, c2, b);
                         }
                     }
-                    if (++g == ngroups) { g = 0; ph ^= 1u; }
+                    if (++g == ngroups) {
+                        g = 0;
+                        ph ^= 1u;
+                        gst = base;
+                    } else {
+                        gst += group_bytes;
+                    }
                 }
             }
             // Every load issued has landed before the CTA may exit (immediate
             // when the consumer already waited for it).
             if (lane == 0) {
-                for (uint32_t q = 0; q < (uint32_t)(p.stages / p.kgroup); ++q) {
+                for (uint32_t q = 0; q < (uint32_t)(p.stages / KG); ++q) {
                     if ((issued_mask >> q) & 1u) {
                         if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
                             report_error(p.err, DEV_TIMEOUT_TEARDOWN);
@@ -149,14 +157,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Descriptors, steps and ring bounds sit in registers: one thread
             // issues every MMA, and its per-K-block instruction latency must
             // stay below the tensor pipe's time for that block.
-            const int kg = p.kgroup;
-            const uint32_t ngroups = (uint32_t)(p.stages / kg);
-            const uint32_t desc_step = p.stage_stride >> 4;
+            const uint32_t ngroups = (uint32_t)(p.stages / KG);
+            const uint64_t stage_desc = p.stage_stride >> 4;
+            const uint64_t group_desc = KG * stage_desc;
             const uint64_t a_desc0 = p.a_desc_hi | (uint64_t)((base >> 4) & 0x3FFFu);
             const uint64_t b_desc0 = p.b_desc_hi | (uint64_t)(((base + p.b_off) >> 4) & 0x3FFFu);
             const uint64_t ak = p.a_kstep >> 4, bk = p.b_kstep >> 4;
             const uint32_t idesc = p.idesc;
             uint32_t g = 0, ph = 0;
+            uint64_t so = 0;                           // group's descriptor offset
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
@@ -168,24 +177,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = 0; kb < p.num_k; kb += kg) {
-                    const int n = min(kg, p.num_k - kb);
+                for (int kb = 0; kb < p.num_k; kb += KG) {
                     if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int j = 0; j < n; ++j) {
-                        const uint64_t so = (uint64_t)((g * (uint32_t)kg + (uint32_t)j) * desc_step);
-                        const uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
-                        umma_f16(d_tmem, ad, bd, idesc, (uint32_t)(kb + j != 0));
+                    uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
+                    umma_f16(d_tmem, ad, bd, idesc, (uint32_t)(kb != 0));
+                    umma_f16(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                    umma_f16(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                    umma_f16(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+                    if (KG == 2 && kb + 1 < p.num_k) {
+                        ad += stage_desc;
+                        bd += stage_desc;
+                        umma_f16(d_tmem, ad, bd, idesc, 1u);
                         umma_f16(d_tmem, ad + ak, bd + bk, idesc, 1u);
                         umma_f16(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
                         umma_f16(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     }
                     umma_commit(empty_bar(g));     // group free once these MMAs retire
-                    if (++g == ngroups) { g = 0; ph ^= 1u; }
+                    if (++g == ngroups) {
+                        g = 0;
+                        ph ^= 1u;
+                        so = 0;
+                    } else {
+                        so += group_desc;
+                    }
                 }
                 if (!ok) break;
                 umma_commit(accf_bar(buf));        // accumulator ready for the epilogue

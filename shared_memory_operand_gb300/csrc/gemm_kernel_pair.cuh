@@ -11,9 +11,8 @@
 // output tiles raise arithmetic intensity; Level 9: a cluster of workgroups
 // shares operand panels instead of re-requesting them).
 //
-// The ring's stages are handed over in groups of `kgroup` (two for the
-// 6-stage ring): one full/empty barrier pair, one wait and one commit per
-// group of 2 x 4 MMAs.  A single thread issues every MMA, and with a wait and
+// The ring's stages are handed over in groups of two: one full/empty barrier
+// pair, one wait and one commit per group of 2 x 4 MMAs.  A single thread issues every MMA, and with a wait and
 // a commit per 4 MMAs its instruction latency, not the tensor pipe, set the
 // pace.
 //
@@ -36,6 +35,7 @@
 namespace smo {
 
 static_assert(kBK / kMmaK == 4, "the issue loop unrolls four MMAs per K block");
+constexpr int kPairGroup = 2;       // stages per full/empty barrier pair (the ring holds 6)
 
 template <int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,9 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((uint32_t)lane < nloads) {
             const uint32_t lmask = (1u << nloads) - 1u;
             const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
-            const int kg = p.kgroup;
-            const uint32_t ngroups = (uint32_t)(p.stages / kg);
-            uint32_t g = 0, ph = 0;
+            const uint32_t ngroups = (uint32_t)(p.stages / kPairGroup);
+            const uint32_t group_bytes = kPairGroup * p.stage_stride;
+            uint32_t g = 0, ph = 0, gst = base;           // group index, ring parity, group's smem
             uint32_t issued_mask = 0, issued_ph = 0;
             bool skip_one = p.stall != 0;
             bool ok = true;
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this CTA's A rows / B columns
                 const int32_t mn0 = slot.is_a ? mb * (2 * kBM) + (int32_t)rank * kBM
                                               : nb * p.BN + (int32_t)rank * half_bn;
-                for (int kb = w.kb0; kb < w.kb1; kb += kg) {
-                    const int n = min(kg, w.kb1 - kb);          // K blocks in this group
+                for (int kb = w.kb0; kb < w.kb1; kb += kPairGroup) {
+                    const bool two = kb + 1 < w.kb1;           // a range's last group may hold one block
                     int good = 1;
                     if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
@@ -126,25 +126,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t fb = mapa_shared(full_bar(g), lead);
                         if (rank == 0 && lane == 0) {
-                            mbar_arrive_expect_tx(full_bar(g), (uint32_t)n * p.tx_bytes);   // both CTAs' bytes
+                            mbar_arrive_expect_tx(full_bar(g), two ? 2 * p.tx_bytes : p.tx_bytes);   // both CTAs
                             issued_mask |= 1u << g;
                             issued_ph = (issued_ph & ~(1u << g)) | (ph << g);
                         }
                         __syncwarp(lmask);
-                        for (int j = 0; j < n; ++j) {
-                            const uint32_t st = base + (g * (uint32_t)kg + (uint32_t)j) * p.stage_stride;
-                            int32_t c0, c1, c2;
-                            slot_coords(slot, mn0, (kb + j) * kBK, c0, c1, c2);
-                            tma_load_4d_pair(st + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
+                        int32_t c0, c1, c2;
+                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
+                        tma_load_4d_pair(gst + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
+                        if (two) {
+                            slot_coords(slot, mn0, (kb + 1) * kBK, c0, c1, c2);
+                            tma_load_4d_pair(gst + p.stage_stride + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
                         }
                     }
-                    if (++g == ngroups) { g = 0; ph ^= 1u; }
+                    if (++g == ngroups) {
+                        g = 0;
+                        ph ^= 1u;
+                        gst = base;
+                    } else {
+                        gst += group_bytes;
+                    }
                 }
             }
             if (lane == 0 && rank == 0) {
                 // Every armed group has received both CTAs' bytes (immediate when
                 // the MMA thread already consumed it).
-                for (uint32_t q = 0; q < (uint32_t)(p.stages / p.kgroup); ++q) {
+                for (uint32_t q = 0; q < (uint32_t)(p.stages / kPairGroup); ++q) {
                     if ((issued_mask >> q) & 1u) {
                         if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
                             report_error(p.err, DEV_TIMEOUT_TEARDOWN);
@@ -165,14 +172,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Everything the issue loop needs sits in registers: the single
             // issuing thread, not the tensor pipe, is the limit when each K
             // block's MMAs wait behind parameter loads and address arithmetic.
-            const int kg = p.kgroup;
-            const uint32_t ngroups = (uint32_t)(p.stages / kg);
-            const uint32_t desc_step = p.stage_stride >> 4;                 // descriptor units per stage
+            const uint32_t ngroups = (uint32_t)(p.stages / kPairGroup);
+            const uint64_t stage_desc = p.stage_stride >> 4;                // descriptor units per stage
+            const uint64_t group_desc = kPairGroup * stage_desc;
             const uint64_t a_desc0 = p.a_desc_hi | (uint64_t)((base >> 4) & 0x3FFFu);
             const uint64_t b_desc0 = p.b_desc_hi | (uint64_t)(((base + p.b_off) >> 4) & 0x3FFFu);
             const uint64_t ak = p.a_kstep >> 4, bk = p.b_kstep >> 4;
             const uint32_t idesc = p.idesc;
             uint32_t g = 0, ph = 0;
+            uint64_t so = 0;                                                 // group's descriptor offset
             uint32_t it = 0;
             bool ok = true;
             WorkIter wi;
@@ -187,24 +195,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = w.kb0; kb < w.kb1; kb += kg) {
-                    const int n = min(kg, w.kb1 - kb);
+                for (int kb = w.kb0; kb < w.kb1; kb += kPairGroup) {
                     if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    for (int j = 0; j < n; ++j) {
-                        const uint64_t so = (uint64_t)((g * (uint32_t)kg + (uint32_t)j) * desc_step);
-                        const uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
-                        umma_f16_pair(d_tmem, ad, bd, idesc, (uint32_t)(kb + j != w.kb0));
+                    uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
+                    umma_f16_pair(d_tmem, ad, bd, idesc, (uint32_t)(kb != w.kb0));
+                    umma_f16_pair(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                    umma_f16_pair(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                    umma_f16_pair(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+                    if (kb + 1 < w.kb1) {
+                        ad += stage_desc;
+                        bd += stage_desc;
+                        umma_f16_pair(d_tmem, ad, bd, idesc, 1u);
                         umma_f16_pair(d_tmem, ad + ak, bd + bk, idesc, 1u);
                         umma_f16_pair(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
                         umma_f16_pair(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     }
                     umma_commit_pair_mc(empty_bar(g), (uint16_t)(3u << lead));   // both CTAs' group g free
-                    if (++g == ngroups) { g = 0; ph ^= 1u; }
+                    if (++g == ngroups) {
+                        g = 0;
+                        ph ^= 1u;
+                        so = 0;
+                    } else {
+                        so += group_desc;
+                    }
                 }
                 if (!ok) break;
                 umma_commit_pair_mc(accf_bar(buf), (uint16_t)(3u << lead));       // both accumulators ready

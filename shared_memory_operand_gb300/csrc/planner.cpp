@@ -229,8 +229,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.stages = stages;
     // Two stages per barrier pair halve the waits and commits the single
     // MMA-issuing thread executes per MMA.  With fewer than six stages the
-    // ring would have too few groups in flight to hide the load latency.
-    p.kgroup = stages >= 6 ? 2 : 1;
+    // one-CTA ring would have too few groups in flight to hide the load
+    // latency; the CTA-pair kernel (32 KiB stages, six of them) always
+    // groups two.
+    if (p.pair && stages < 4) {
+        p.why = "shared memory too small for two groups of two stages";
+        return p;
+    }
+    p.kgroup = (p.pair || stages >= 6) ? 2 : 1;
     p.off_epi = stages * p.stage_stride;
     p.off_bar = p.off_epi + epi_bytes;
     p.smem_bytes = p.off_bar + kBarrierBytes + 1024;
