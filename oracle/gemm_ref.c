@@ -14,8 +14,9 @@
  *   C_ref[b][m][n] = sum_{k = 0 .. K-1} A[b][m][k] * B[b][k][n]
  *
  * evaluated in IEEE double with k ascending for every element, no fused
- * multiply-add (build with -ffp-contract=off), from the 16-bit operand bit
- * patterns the GPU reads.  The loop nest walks n innermost so that each
+ * multiply-add (build with -ffp-contract=off), from the operand bit patterns
+ * the GPU reads (16-bit formats as uint16 arrays, 8-bit formats as uint8
+ * arrays).  The loop nest walks n innermost so that each
  * element's partial sum still receives its terms in ascending k; the per-element
  * arithmetic is exactly the dot product above.
  *
@@ -26,8 +27,17 @@
  *   B N-major : B[b][k][n] at b[b*sb + k*ldb + n]
  *   C         : C[b][m][n] at c[b*sc + m*ldc + n]
  *
+ *   "An Educational GEMM Ladder for Helios GPUs", section "Educational GEMM
+ *   Ladder": the matrix units take BF16, FP8, FP6 and FP4 operands; "A Deep
+ *   Dive into LDS Optimizations on AMD Instinct MI450 GPUs", Part I: the 8-bit
+ *   transposed operand load (ds_load_tr8_b64).  The 8-bit operand product is the
+ *   same definition over FP8 inputs.
+ *
  * 16-bit formats (IEEE 754-2008 binary16, and bfloat16 = the top half of
- * binary32) are decoded from their bit fields here, and doubles are rounded to
+ * binary32) and the two 8-bit formats of the OCP 8-bit floating point
+ * specification (E4M3: bias 7, no infinities, S.1111.111 is NaN; E5M2: bias 15,
+ * IEEE-style infinities and NaNs) are decoded from their bit fields here, and
+ * doubles are rounded to
  * binary32 / bfloat16 / binary16 by round-to-nearest, ties-to-even, written
  * from the standard's definition: scale by the quantum of the target binade,
  * round the (exact) quotient to an integer with nearbyint() under the default
@@ -41,7 +51,7 @@
 #include <omp.h>
 #endif
 
-enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2 };
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4 };
 
 /* ---- decoding ------------------------------------------------------------ */
 
@@ -84,6 +94,59 @@ double orc_decode16(uint16_t h, int dtype) {
 
 void orc_decode16_array(const uint16_t* h, int64_t n, int dtype, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_decode16(h[i], dtype);
+}
+
+/* E4M3: sign 1 | exponent 4 (bias 7) | fraction 3.  Exponent field 0 holds the
+ * subnormals f * 2^(1-7-3); the all-ones exponent is an ordinary binade except
+ * for fraction 111, the only NaN (no infinities), so the largest value is
+ * 1.110b * 2^8 = 448. */
+static double e4m3_bits_to_f64(uint8_t h) {
+    int sign = (h >> 7) & 1;
+    int e = (h >> 3) & 0xF;
+    int f = h & 0x7;
+    double v;
+    if (e == 0xF && f == 0x7) {
+        v = NAN;
+    } else if (e == 0) {
+        v = ldexp((double)f, 1 - 7 - 3);
+    } else {
+        v = ldexp((double)(8 + f), e - 7 - 3);          /* 1.f * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+/* E5M2: sign 1 | exponent 5 (bias 15) | fraction 2, with IEEE 754 conventions:
+ * exponent 0 is subnormal, all-ones exponent is infinity (fraction 0) or NaN. */
+static double e5m2_bits_to_f64(uint8_t h) {
+    int sign = (h >> 7) & 1;
+    int e = (h >> 2) & 0x1F;
+    int f = h & 0x3;
+    double v;
+    if (e == 0x1F) {
+        v = f ? NAN : INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)f, 1 - 15 - 2);
+    } else {
+        v = ldexp((double)(4 + f), e - 15 - 2);         /* 1.f * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+double orc_decode8(uint8_t h, int dtype) {
+    return dtype == ORC_E4M3 ? e4m3_bits_to_f64(h) : e5m2_bits_to_f64(h);
+}
+
+void orc_decode8_array(const uint8_t* h, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_decode8(h[i], dtype);
+}
+
+/* Bytes per operand element of an input format. */
+int orc_elem_bytes(int dtype) { return (dtype == ORC_E4M3 || dtype == ORC_E5M2) ? 1 : 2; }
+
+/* Element idx of an operand array of the given input format. */
+static inline double operand_at(const void* p, int64_t idx, int dtype) {
+    if (dtype == ORC_E4M3 || dtype == ORC_E5M2) return orc_decode8(((const uint8_t*)p)[idx], dtype);
+    return orc_decode16(((const uint16_t*)p)[idx], dtype);
 }
 
 /* ---- rounding ------------------------------------------------------------ */
@@ -149,22 +212,22 @@ void orc_round_array(const double* in, int64_t n, int out_dtype, double* out) {
 
 /* ---- the GEMM ------------------------------------------------------------ */
 
-static inline double a_at(const uint16_t* a, int dt, int a_mn_major, int64_t lda,
+static inline double a_at(const void* a, int dt, int a_mn_major, int64_t lda,
                           int64_t sa, int64_t b, int64_t m, int64_t k) {
     int64_t idx = b * sa + (a_mn_major ? k * lda + m : m * lda + k);
-    return orc_decode16(a[idx], dt);
+    return operand_at(a, idx, dt);
 }
 
-static inline double b_at(const uint16_t* bm, int dt, int b_mn_major, int64_t ldb,
+static inline double b_at(const void* bm, int dt, int b_mn_major, int64_t ldb,
                           int64_t sb, int64_t b, int64_t k, int64_t n) {
     int64_t idx = b * sb + (b_mn_major ? k * ldb + n : n * ldb + k);
-    return orc_decode16(bm[idx], dt);
+    return operand_at(bm, idx, dt);
 }
 
 /* Full product into a dense fp64 array c[b][m][n] (row-major, ld = N).
  * Returns 0, or -1 if scratch could not be allocated. */
-int orc_gemm_f64(const uint16_t* a, int64_t lda, int a_mn_major,
-                 const uint16_t* bmat, int64_t ldb, int b_mn_major,
+int orc_gemm_f64(const void* a, int64_t lda, int a_mn_major,
+                 const void* bmat, int64_t ldb, int b_mn_major,
                  int in_dtype, int64_t M, int64_t N, int64_t K,
                  int64_t batch, int64_t sa, int64_t sb, double* c) {
     int err = 0;
@@ -196,8 +259,8 @@ int orc_gemm_f64(const uint16_t* a, int64_t lda, int a_mn_major,
 /* Selected elements only: out[i] = C_ref[bi[i]][mi[i]][ni[i]], each one a plain
  * dot product with k ascending (used to check full-size GPU results at sampled
  * positions). */
-void orc_gemm_f64_sampled(const uint16_t* a, int64_t lda, int a_mn_major,
-                          const uint16_t* bmat, int64_t ldb, int b_mn_major,
+void orc_gemm_f64_sampled(const void* a, int64_t lda, int a_mn_major,
+                          const void* bmat, int64_t ldb, int b_mn_major,
                           int in_dtype, int64_t K, int64_t sa, int64_t sb,
                           const int64_t* bi, const int64_t* mi, const int64_t* ni,
                           int64_t count, double* out) {

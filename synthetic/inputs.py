@@ -1,15 +1,17 @@
 """Seeded operand generation (CPU, torch.Generator) for the GEMM workloads.
 
 Recipe (one generator per problem, seeded, draws A then B):
-  uniform : torch.rand * 2 - 1 in fp32, rounded to the 16-bit input type
+  uniform : torch.rand * 2 - 1 in fp32, rounded to the input type
+            (bf16 / f16, or FP8 E4M3 / E5M2, by torch's round-to-nearest-even)
   normal  : torch.randn * sigma in fp32, rounded likewise
-  int     : torch.randint(-4, 5) (integers in [-4, 4]), exact in bf16/f16
+  int     : torch.randint(-4, 5) (integers in [-4, 4]), exact in every input type
 Logical A is batch x M x K and logical B is batch x K x N; each is then stored
 in the requested orientation:
   A K-major: rows of K (lda >= K)      A M-major: rows of M (lda >= M)
   B K-major: rows of K, one per n      B N-major: rows of N, one per k
 Leading dimensions are padded up to ``ld_align`` elements (TMA needs 16-byte
-row pitches); padding cells hold a poison value the product must never read.
+row pitches: 8 elements of 16 bits, 16 of 8 bits); padding cells hold a poison
+value the product must never read (4096, or 448 = the largest E4M3 value).
 """
 from __future__ import annotations
 
@@ -19,8 +21,15 @@ from typing import Dict, Optional
 import torch
 
 K_MAJOR, MN_MAJOR = 0, 1
-_TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+_TORCH_DT = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32,
+             "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+FP8 = ("e4m3", "e5m2")
 POISON = 4096.0
+_POISON = {"e4m3": 448.0}
+
+
+def elem_bytes(dtype: str) -> int:
+    return {"bf16": 2, "f16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}[dtype]
 
 
 @dataclass
@@ -33,7 +42,7 @@ class Problem:
     b_major: int
     in_dtype: str
     out_dtype: str
-    A: torch.Tensor            # CPU storage, 1-D, 16-bit
+    A: torch.Tensor            # CPU storage, 1-D, 16-bit or 8-bit
     B: torch.Tensor
     lda: int
     ldb: int
@@ -53,8 +62,11 @@ class Problem:
         return self.batch * self.strideC if self.batch > 1 else self.M * self.ldc
 
     def bits(self, which: str):
-        """Operand storage as a numpy uint16 array (the oracle's input)."""
+        """Operand storage as a numpy uint16 (16-bit types) or uint8 (FP8)
+        array: the oracle's input."""
         t = self.A if which == "A" else self.B
+        if self.in_dtype in FP8:
+            return t.view(torch.uint8).numpy()
         return t.view(torch.int16).numpy().view("uint16")
 
     def logical_A(self) -> torch.Tensor:
@@ -89,7 +101,8 @@ def _draw(gen: torch.Generator, shape, dist: str, sigma: float) -> torch.Tensor:
     raise ValueError(dist)
 
 
-def _store(logical: torch.Tensor, mn_major: bool, ld: int, dt: torch.dtype) -> (torch.Tensor, int):
+def _store(logical: torch.Tensor, mn_major: bool, ld: int, dt: torch.dtype,
+           poison: float = POISON) -> (torch.Tensor, int):
     """logical: batch x R x Kd (R = M for A, N for B).  Returns 1-D storage and
     the batch stride."""
     batch, R, Kd = logical.shape
@@ -100,25 +113,28 @@ def _store(logical: torch.Tensor, mn_major: bool, ld: int, dt: torch.dtype) -> (
         rows, cols = Kd, R
         src = logical.transpose(1, 2)
     stride = rows * ld
-    buf = torch.full((batch, rows, ld), POISON, dtype=torch.float32)
+    buf = torch.full((batch, rows, ld), poison, dtype=torch.float32)
     buf[:, :, :cols] = src
     return buf.to(dt).reshape(-1).contiguous(), stride
 
 
 def make_problem(M: int, N: int, K: int, *, a_major: int = K_MAJOR, b_major: int = MN_MAJOR,
                  in_dtype: str = "bf16", out_dtype: str = "bf16", dist: str = "uniform",
-                 sigma: float = 1.0, seed: int = 0, batch: int = 1, ld_align: int = 8,
+                 sigma: float = 1.0, seed: int = 0, batch: int = 1, ld_align: Optional[int] = None,
                  ld_extra: int = 0) -> Problem:
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
     dt = _TORCH_DT[in_dtype]
+    if ld_align is None:
+        ld_align = 16 // elem_bytes(in_dtype)
+    poison = _POISON.get(in_dtype, POISON)
     a_log = _draw(gen, (batch, M, K), dist, sigma).to(dt).to(torch.float32)
     b_log = _draw(gen, (batch, K, N), dist, sigma).to(dt).to(torch.float32)
     lda = _round_up((M if a_major == MN_MAJOR else K) + ld_extra, ld_align)
     ldb = _round_up((N if b_major == MN_MAJOR else K) + ld_extra, ld_align)
-    A, sA = _store(a_log, a_major == MN_MAJOR, lda, dt)
+    A, sA = _store(a_log, a_major == MN_MAJOR, lda, dt, poison)
     # B logical batch x K x N; stored per n (K-major) or per k (N-major)
-    B, sB = _store(b_log.transpose(1, 2), b_major == MN_MAJOR, ldb, dt)
+    B, sB = _store(b_log.transpose(1, 2), b_major == MN_MAJOR, ldb, dt, poison)
     out_align = 4 if out_dtype == "f32" else 8
     ldc = _round_up(N, out_align)
     return Problem(M, N, K, batch, a_major, b_major, in_dtype, out_dtype, A, B, lda, ldb, ldc,
@@ -153,6 +169,12 @@ WORKLOADS: Dict[str, Dict] = {
     "batched_32x2048_bf16": dict(M=2048, N=2048, K=2048, batch=32, a_major=K_MAJOR,
                                  b_major=MN_MAJOR, in_dtype="bf16", out_dtype="bf16",
                                  dist="normal", sigma=0.02),
+    # 8-bit operands (E4M3), fp32 accumulate, bf16 out: the 8192^3 shape in the
+    # transposed-B orientation and K-major B
+    "gemm_8192_e4m3_bf16_AK_BN": dict(M=8192, N=8192, K=8192, a_major=K_MAJOR, b_major=MN_MAJOR,
+                                      in_dtype="e4m3", out_dtype="bf16", dist="uniform"),
+    "gemm_8192_e4m3_bf16_AK_BK": dict(M=8192, N=8192, K=8192, a_major=K_MAJOR, b_major=K_MAJOR,
+                                      in_dtype="e4m3", out_dtype="bf16", dist="uniform"),
 }
 
 
