@@ -2,11 +2,14 @@
  * smo_gemm.h -- C ABI of the shared-memory-operand GEMM library (libsmo_gemm.so)
  *
  * One operation: the dense matrix product C = A * B with 16-bit operands
- * (bfloat16 or float16), fp32 accumulation in tensor memory, and fp32 / bf16 /
+ * (bfloat16 or float16) or 8-bit floating-point operands (FP8 E4M3 or E5M2 of
+ * the OCP 8-bit format), fp32 accumulation in tensor memory, and fp32 / bf16 /
  * f16 output.  Source of the operation: "An Educational GEMM Ladder for Helios
  * GPUs", section "Educational GEMM Ladder" (every rung computes C = AB with
- * A in R^{MxK}, B in R^{KxN}, BF16 inputs); the f16 variant is the GEMM of
- * rocMLIR pull 2196's description (-m 1500 -n 1152 -k 896, f16).  Operands are
+ * A in R^{MxK}, B in R^{KxN}, BF16 inputs, on matrix units that also take
+ * FP8); the f16 variant is the GEMM of rocMLIR pull 2196's description
+ * (-m 1500 -n 1152 -k 896, f16); the 8-bit operands are those of the 8-bit
+ * transposed load of the MI450 post, Part I (ds_load_tr8_b64).  Operands are
  * staged through shared memory in 128-byte-swizzled layouts, and an
  * N-contiguous ("transposed") B is consumed directly -- the role that
  * "A Deep Dive into LDS Optimizations on AMD Instinct MI450 GPUs", Part I
@@ -47,7 +50,7 @@ extern "C" {
 #endif
 
 typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
-typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+typedef enum { GEMM_BF16 = 0, GEMM_F16 = 1, GEMM_F32 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4 } gemm_dtype_t;
 
 typedef enum {
     GEMM_OK = 0,
@@ -73,7 +76,9 @@ int gemm_bf16(const void* A, int64_t lda, int a_major,
 
 /*
  * gemm_ex: general entry point.
- * in_dtype : GEMM_BF16 or GEMM_F16 (A and B share it).
+ * in_dtype : GEMM_BF16, GEMM_F16, GEMM_E4M3 or GEMM_E5M2 (A and B share it;
+ *            FP8 operands are one byte per element, so lda / ldb / strides
+ *            must be multiples of 16 elements).
  * out_dtype: GEMM_F32, GEMM_BF16 or GEMM_F16 (fp32 accumulator rounded to
  *            nearest-even on output).
  * batch >= 1 independent problems; strideA/B/C are ignored when batch == 1.

@@ -16,12 +16,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libsmo_gemm.so")
 
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
-GEMM_BF16, GEMM_F16, GEMM_F32 = 0, 1, 2
+GEMM_BF16, GEMM_F16, GEMM_F32, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
 GEMM_OK = 0
 GEMM_ERR_ARG, GEMM_ERR_ALIGN, GEMM_ERR_UNSUPPORTED = -1, -2, -3
 GEMM_ERR_LAUNCH, GEMM_ERR_TIMEOUT, GEMM_ERR_CUDA, GEMM_ERR_NO_DEVICE = -4, -5, -6, -7
 
-DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32}
+DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32, "e4m3": GEMM_E4M3, "e5m2": GEMM_E5M2}
 
 # Every symbol include/smo_gemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_ex", "gemm_check", "gemm_status_string", "gemm_set_timeout_ns",

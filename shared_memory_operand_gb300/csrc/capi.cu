@@ -33,8 +33,8 @@ struct DevState {
     bool usable = false;
     int num_sms = 0;
     int32_t* d_err = nullptr;
-    bool attr_set[6] = {false, false, false, false, false, false};   // [OUT * 2 + KG - 1]
-    bool pair_attr_set[3] = {false, false, false};
+    bool attr_set[12] = {};         // one-CTA kernels: [(KIND * 3 + OUT) * 2 + KG - 1]
+    bool pair_attr_set[6] = {};     // pair kernels: [KIND * 3 + OUT]
     int pair_max_clusters[3] = {0, 0, 0};   // co-resident 2-CTA clusters of the pair kernel
     // Stream-K workspace, one per stream so that GEMMs running concurrently
     // on different streams never share partial slots or tile counters.
@@ -54,11 +54,14 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 using PlanKey = std::tuple<int64_t, int64_t, int64_t, int, int, int, int, int64_t, int, int>;
 std::map<PlanKey, Plan> g_plans;
 
-int elem_size(int dt) { return dt == GEMM_F32 ? 4 : 2; }
+int elem_size(int dt) { return dt == GEMM_F32 ? 4 : (dt == GEMM_E4M3 || dt == GEMM_E5M2) ? 1 : 2; }
+bool is_fp8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
 
+// TMA moves FP8 operands as plain bytes; only the tensor core interprets them.
 CUtensorMapDataType tmap_type(int dt) {
     return dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
          : dt == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+         : is_fp8(dt)     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
 }
 
@@ -137,7 +140,7 @@ int validate(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_d
     if ((a_major != GEMM_K_MAJOR && a_major != GEMM_MN_MAJOR) ||
         (b_major != GEMM_K_MAJOR && b_major != GEMM_MN_MAJOR))
         return GEMM_ERR_ARG;
-    if (in_dtype != GEMM_BF16 && in_dtype != GEMM_F16) return GEMM_ERR_UNSUPPORTED;
+    if (in_dtype != GEMM_BF16 && in_dtype != GEMM_F16 && !is_fp8(in_dtype)) return GEMM_ERR_UNSUPPORTED;
     if (out_dtype != GEMM_BF16 && out_dtype != GEMM_F16 && out_dtype != GEMM_F32) return GEMM_ERR_UNSUPPORTED;
     if (M >= (1ll << 31) || N >= (1ll << 31) || K >= (1ll << 31) || batch >= (1ll << 31))
         return GEMM_ERR_UNSUPPORTED;
@@ -192,14 +195,14 @@ int encode_box(CUtensorMap* m, int dt, const void* ptr, uint64_t inner, uint64_t
 }
 
 // MN-major operand whose per-stage boxes are loaded by one instruction:
-// {64 (contiguous), K, MN / 64, batch}; needs MN % 64 == 0 so that no box
-// reaches past the operand's extent.
+// {T (contiguous, 128 bytes), K, MN / T, batch}; needs MN % T == 0 so that no
+// box reaches past the operand's extent.
 int encode_fused(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t k, uint64_t batch, uint64_t ld,
-                 uint64_t stride, uint32_t nbox) {
+                 uint64_t stride, uint32_t nbox, uint32_t T, uint32_t bk) {
     const uint64_t es = (uint64_t)elem_size(dt);
-    cuuint64_t dims[4] = {64, k, mn / 64, batch};
-    cuuint64_t strides[3] = {ld * es, 64 * es, batch_stride_bytes(es, ld, k, batch, stride)};
-    cuuint32_t box[4] = {64, (cuuint32_t)smo::kBK, nbox, 1};
+    cuuint64_t dims[4] = {T, k, mn / T, batch};
+    cuuint64_t strides[3] = {ld * es, T * es, batch_stride_bytes(es, ld, k, batch, stride)};
+    cuuint32_t box[4] = {T, bk, nbox, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, tmap_type(dt), 4, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -207,38 +210,39 @@ int encode_fused(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t 
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
 }
 
-template <int OUT, int KG>
+template <int OUT, int KG, int KIND>
 int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
                      const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
-    auto kern = smo::smo_gemm_kernel<OUT, KG>;
-    if (!ds.attr_set[OUT * 2 + KG - 1]) {
+    auto kern = smo::smo_gemm_kernel<OUT, KG, KIND>;
+    const int slot = (KIND * 3 + OUT) * 2 + KG - 1;
+    if (!ds.attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
             cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
-        ds.attr_set[OUT * 2 + KG - 1] = true;
+        ds.attr_set[slot] = true;
     }
     kern<<<pl.grid, smo::kThreads, pl.smem_bytes, stream>>>(ta, tb, tc, kp);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }
 
-template <int OUT>
+template <int OUT, int KIND>
 int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
                   const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
-    return kp.kgroup == 2 ? launch_single_kg<OUT, 2>(pl, ds, ta, tb, tc, kp, stream)
-                          : launch_single_kg<OUT, 1>(pl, ds, ta, tb, tc, kp, stream);
+    return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND>(pl, ds, ta, tb, tc, kp, stream)
+                          : launch_single_kg<OUT, 1, KIND>(pl, ds, ta, tb, tc, kp, stream);
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM; the persistent grid is
 // as many clusters as can be co-resident.  With stream-K the whole tiles are
 // dealt round-robin and the K blocks of the last, partial wave's tiles are
 // shared out evenly, so that every cluster ends at the same time.
-template <int OUT>
+template <int OUT, int KIND>
 int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 KParams kp, cudaStream_t stream, int stream_k) {
-    auto kern = smo::smo_gemm_pair_kernel<OUT>;
+    auto kern = smo::smo_gemm_pair_kernel<OUT, KIND>;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];
@@ -251,7 +255,7 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!ds.pair_attr_set[OUT]) {
+    if (!ds.pair_attr_set[KIND * 3 + OUT]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
             cudaSuccess) {
             cudaGetLastError();
@@ -264,7 +268,7 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
             return GEMM_ERR_LAUNCH;
         }
         ds.pair_max_clusters[OUT] = n;
-        ds.pair_attr_set[OUT] = true;
+        ds.pair_attr_set[KIND * 3 + OUT] = true;
     }
     const int64_t maxc = ds.pair_max_clusters[OUT];
     int64_t clusters = std::min<int64_t>(pl.tiles, maxc);
@@ -337,11 +341,18 @@ no_stream_k:
     return GEMM_OK;
 }
 
+template <int OUT, int KIND>
+int launch_kind(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const KParams& kp, cudaStream_t stream, int stream_k) {
+    return pl.pair ? launch_pair<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream, stream_k)
+                   : launch_single<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream);
+}
+
 template <int OUT>
 int launch(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
            const KParams& kp, cudaStream_t stream, int stream_k) {
-    return pl.pair ? launch_pair<OUT>(pl, ds, ta, tb, tc, kp, stream, stream_k)
-                   : launch_single<OUT>(pl, ds, ta, tb, tc, kp, stream);
+    return pl.kind == smo::KIND_F8F6F4 ? launch_kind<OUT, smo::KIND_F8F6F4>(pl, ds, ta, tb, tc, kp, stream, stream_k)
+                                       : launch_kind<OUT, smo::KIND_F16>(pl, ds, ta, tb, tc, kp, stream, stream_k);
 }
 
 // ---------------------------------------------------------------------------
@@ -455,12 +466,15 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     const int64_t a_outer = (a_major == GEMM_MN_MAJOR) ? K : M;
     const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
     CUtensorMap ta, tb, tc;
-    // MN-major operands whose extent is a multiple of 64 take one 4-D load per
-    // stage instead of one load per 64-wide box.
-    const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % 64 == 0 &&
-                         encode_fused(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox) == GEMM_OK;
-    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % 64 == 0 &&
-                         encode_fused(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox) == GEMM_OK;
+    // MN-major operands whose extent is a multiple of the 128-byte box width
+    // take one 4-D load per stage instead of one load per box.
+    const uint32_t aT = pl->a.box_inner, bT = pl->b.box_inner;
+    const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % aT == 0 &&
+                         encode_fused(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox, aT,
+                                      (uint32_t)pl->bk) == GEMM_OK;
+    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % bT == 0 &&
+                         encode_fused(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox, bT,
+                                      (uint32_t)pl->bk) == GEMM_OK;
     if ((!a_fused &&
          encode_box(&ta, in_dtype, A, a_row, a_outer, batch, lda, strideA, pl->a.box_inner, pl->a.box_outer)) ||
         (!b_fused &&

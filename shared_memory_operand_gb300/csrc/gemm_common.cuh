@@ -33,15 +33,17 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int64_t t, int& b,
 // One TMA load of a pipeline stage, owned by one lane of the producer warp.
 // All of a stage's loads (A boxes, then B boxes) are issued by consecutive
 // lanes in a single instruction: the producer's issue cost is then one
-// instruction per stage instead of one per box.  Every operand map is 4-D:
-//   fused MN-major (extent % 64 == 0): {64, K, MN / 64, batch}, one load
-//   K-major box:                       {K, MN, 1, batch}
-//   MN-major 64-wide box:              {MN, K, 1, batch}
+// instruction per stage instead of one per box.  Every operand map is 4-D;
+// T = 128 bytes of MN elements (64 of 16 bits, 128 of 8 bits):
+//   fused MN-major (extent % T == 0): {T, K, MN / T, batch}, one load
+//   K-major box:                      {K, MN, 1, batch}
+//   MN-major T-wide box:              {MN, K, 1, batch}
 struct LoadSlot {
     const CUtensorMap* tm;
     uint32_t dst_off;      // from the stage base
     uint32_t mode;         // 0 fused, 1 K-major box, 2 MN-major box
     int32_t mn_off;        // offset of this box along MN
+    int32_t box_mn;        // MN extent of one box
     bool is_a;
 };
 
@@ -60,7 +62,8 @@ __device__ __forceinline__ LoadSlot load_slot(const KParams& p, const CUtensorMa
     s.tm = s.is_a ? tmA : tmB;
     s.dst_off = (s.is_a ? 0u : p.b_off) + j * (s.is_a ? p.a_box_bytes : p.b_box_bytes);
     s.mode = fused ? 0u : (mn_major ? 2u : 1u);
-    s.mn_off = (int32_t)(j * (s.is_a ? p.a_box_mn : p.b_box_mn));
+    s.box_mn = (int32_t)(s.is_a ? p.a_box_mn : p.b_box_mn);
+    s.mn_off = (int32_t)j * s.box_mn;
     return s;
 }
 
@@ -69,7 +72,7 @@ __device__ __forceinline__ LoadSlot load_slot(const KParams& p, const CUtensorMa
 __device__ __forceinline__ void slot_coords(const LoadSlot& s, int32_t mn0, int32_t k0, int32_t& c0, int32_t& c1,
                                             int32_t& c2) {
     if (s.mode == 0) {
-        c0 = 0; c1 = k0; c2 = mn0 / 64;
+        c0 = 0; c1 = k0; c2 = mn0 / s.box_mn;
     } else if (s.mode == 1) {
         c0 = k0; c1 = mn0 + s.mn_off; c2 = 0;
     } else {

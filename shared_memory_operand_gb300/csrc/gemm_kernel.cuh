@@ -37,10 +37,10 @@
 
 namespace smo {
 
-static_assert(kBK / kMmaK == 4, "the issue loops unroll four MMAs per K block");
+static_assert(kStageKBytes / kMmaKBytes == 4, "the issue loops unroll four MMAs per K block");
 
-// KG: stages per full/empty barrier pair (1 or 2).
-template <int OUT, int KG>
+// KG: stages per full/empty barrier pair (1 or 2).  KIND: MmaKind.
+template <int OUT, int KG, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
@@ -123,10 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp(lmask);
                         int32_t c0, c1, c2;
-                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
+                        slot_coords(slot, mn0, kb * p.bk, c0, c1, c2);
                         tma_load_4d(gst + slot.dst_off, slot.tm, full_bar(g), c0, c1, c2, b);
                         if (two) {
-                            slot_coords(slot, mn0, (kb + 1) * kBK, c0, c1, c2);
+                            slot_coords(slot, mn0, (kb + 1) * p.bk, c0, c1, c2);
                             tma_load_4d(gst + p.stage_stride + slot.dst_off, slot.tm, full_bar(g), c0, c1, c2, b);
                         }
                     }
@@ -185,17 +185,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
-                    umma_f16(d_tmem, ad, bd, idesc, (uint32_t)(kb != 0));
-                    umma_f16(d_tmem, ad + ak, bd + bk, idesc, 1u);
-                    umma_f16(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
-                    umma_f16(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+                    umma<KIND>(d_tmem, ad, bd, idesc, (uint32_t)(kb != 0));
+                    umma<KIND>(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                    umma<KIND>(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                    umma<KIND>(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     if (KG == 2 && kb + 1 < p.num_k) {
                         ad += stage_desc;
                         bd += stage_desc;
-                        umma_f16(d_tmem, ad, bd, idesc, 1u);
-                        umma_f16(d_tmem, ad + ak, bd + bk, idesc, 1u);
-                        umma_f16(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
-                        umma_f16(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+                        umma<KIND>(d_tmem, ad, bd, idesc, 1u);
+                        umma<KIND>(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                        umma<KIND>(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                        umma<KIND>(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     }
                     umma_commit(empty_bar(g));     // group free once these MMAs retire
                     if (++g == ngroups) {

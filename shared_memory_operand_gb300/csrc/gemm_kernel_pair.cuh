@@ -34,10 +34,11 @@
 
 namespace smo {
 
-static_assert(kBK / kMmaK == 4, "the issue loop unrolls four MMAs per K block");
+static_assert(kStageKBytes / kMmaKBytes == 4, "the issue loop unrolls four MMAs per K block");
 constexpr int kPairGroup = 2;       // stages per full/empty barrier pair (the ring holds 6)
 
-template <int OUT>
+// KIND: MmaKind (kind::f16 for 16-bit operands, kind::f8f6f4 for FP8).
+template <int OUT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
@@ -132,10 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp(lmask);
                         int32_t c0, c1, c2;
-                        slot_coords(slot, mn0, kb * kBK, c0, c1, c2);
+                        slot_coords(slot, mn0, kb * p.bk, c0, c1, c2);
                         tma_load_4d_pair(gst + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
                         if (two) {
-                            slot_coords(slot, mn0, (kb + 1) * kBK, c0, c1, c2);
+                            slot_coords(slot, mn0, (kb + 1) * p.bk, c0, c1, c2);
                             tma_load_4d_pair(gst + p.stage_stride + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
                         }
                     }
@@ -203,17 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
-                    umma_f16_pair(d_tmem, ad, bd, idesc, (uint32_t)(kb != w.kb0));
-                    umma_f16_pair(d_tmem, ad + ak, bd + bk, idesc, 1u);
-                    umma_f16_pair(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
-                    umma_f16_pair(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+                    umma_pair<KIND>(d_tmem, ad, bd, idesc, (uint32_t)(kb != w.kb0));
+                    umma_pair<KIND>(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                    umma_pair<KIND>(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                    umma_pair<KIND>(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     if (kb + 1 < w.kb1) {
                         ad += stage_desc;
                         bd += stage_desc;
-                        umma_f16_pair(d_tmem, ad, bd, idesc, 1u);
-                        umma_f16_pair(d_tmem, ad + ak, bd + bk, idesc, 1u);
-                        umma_f16_pair(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
-                        umma_f16_pair(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+                        umma_pair<KIND>(d_tmem, ad, bd, idesc, 1u);
+                        umma_pair<KIND>(d_tmem, ad + ak, bd + bk, idesc, 1u);
+                        umma_pair<KIND>(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+                        umma_pair<KIND>(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
                     }
                     umma_commit_pair_mc(empty_bar(g), (uint16_t)(3u << lead));   // both CTAs' group g free
                     if (++g == ngroups) {

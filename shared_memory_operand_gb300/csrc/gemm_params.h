@@ -6,8 +6,9 @@
 namespace smo {
 
 constexpr int kBM = 128;            // output rows per tile (tcgen05 M, cta_group::1)
-constexpr int kBK = 64;             // K per pipeline stage: 64 x 16-bit = one 128-byte swizzle row
-constexpr int kMmaK = 16;           // K per tcgen05.mma.kind::f16
+constexpr int kStageKBytes = 128;   // K bytes per pipeline stage: one 128-byte swizzle row
+                                    // (64 bf16 / f16 values, 128 FP8 values)
+constexpr int kMmaKBytes = 32;      // K bytes per tcgen05.mma (kind::f16 K = 16, kind::f8f6f4 K = 32)
 constexpr int kThreads = 192;       // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
 constexpr int kEpiWarps = 4;
 constexpr int kEpiRowsPerWarp = 32;
@@ -19,6 +20,9 @@ constexpr uint32_t kBarrierBytes = 256;
 
 // Out element types.
 enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
+
+// tcgen05.mma instruction kinds: 16-bit operands, or 8-bit floating point.
+enum MmaKind { KIND_F16 = 0, KIND_F8F6F4 = 1 };
 
 // Error codes written to the device error word (first writer wins).
 enum DevErr : int32_t {
@@ -37,6 +41,7 @@ struct KParams {
     int64_t tiles_per_batch, total_tiles;
     int32_t BN, stages;
     int32_t kgroup;                 // K blocks (stages) per full/empty barrier pair: 1 or 2
+    int32_t bk;                     // K elements per stage (128 / input element bytes)
     uint32_t idesc;                 // tcgen05 instruction descriptor
     uint32_t a_mn_major, b_mn_major;
     uint32_t a_nbox, b_nbox;        // TMA boxes per stage and operand

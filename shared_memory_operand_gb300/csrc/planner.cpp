@@ -27,27 +27,29 @@ int log2i(uint32_t v) {
 // a stage tile.
 uint32_t tma_offset(const OperandPlan& op, uint32_t mn, uint32_t k) {
     if (!op.mn_major) {
-        // one box: outer = mn rows of 128 bytes (64 k values)
-        return sw128(mn * kSwizzleSpan + k * 2);
+        // one box: outer = mn rows of 128 bytes (bk k values)
+        return sw128(mn * kSwizzleSpan + k * op.es);
     }
-    // boxes of 64 mn x 64 k: box j = mn / 64, row = k, byte = 2 * (mn % 64)
-    uint32_t j = mn / 64;
-    return j * op.box_bytes + sw128(k * kSwizzleSpan + (mn % 64) * 2);
+    // boxes of T = 128 / es mn values x bk k rows: box j = mn / T, row = k
+    const uint32_t T = kSwizzleSpan / op.es;
+    uint32_t j = mn / T;
+    return j * op.box_bytes + sw128(k * kSwizzleSpan + (mn % T) * op.es);
 }
 
 // Where the tensor core reads element (mn, k) given the descriptor fields
 // (canonical SWIZZLE_128B layouts of the tcgen05 shared-memory descriptor),
-// the start address advanced by kstep per 16-wide K step.
+// the start address advanced by kstep per MMA-wide K step.
 uint32_t umma_offset(const OperandPlan& op, uint32_t mn, uint32_t k) {
-    uint32_t step = k / kMmaK, kk = k % kMmaK;
+    uint32_t step = k / op.mma_k, kk = k % op.mma_k;
     uint32_t start = step * op.kstep;
     uint32_t pre;
     if (!op.mn_major) {
         // ((8,m),(T,2)) : ((8T,SBO),(1,T)), T = 16 bytes
-        pre = start + (mn % 8) * 128 + (mn / 8) * op.sbo + kk * 2;
+        pre = start + (mn % 8) * 128 + (mn / 8) * op.sbo + kk * op.es;
     } else {
-        // ((T,8,m),(8,2)) : ((1,T,LBO),(8T,SBO))
-        pre = start + (mn % 64) * 2 + (mn / 64) * op.lbo + (kk % 8) * 128 + (kk / 8) * op.sbo;
+        // ((T,8,m),(8,k)) : ((1,T,LBO),(8T,SBO)), T = 128 bytes of mn
+        const uint32_t T = kSwizzleSpan / op.es;
+        pre = start + (mn % T) * op.es + (mn / T) * op.lbo + (kk % 8) * 128 + (kk / 8) * op.sbo;
     }
     return sw128(pre);
 }
@@ -61,58 +63,66 @@ uint64_t desc_hi(uint32_t lbo, uint32_t sbo) {
     return d;                                        // base offset 0 (1024-aligned stages)
 }
 
-void plan_operand(OperandPlan& op, int mn_major, int tile_mn) {
+// es: bytes per element.  A stage holds one 128-byte swizzle row of K per
+// K-major row (bk = 128 / es) and one MMA consumes 32 bytes of K.
+void plan_operand(OperandPlan& op, int mn_major, int tile_mn, int es) {
     op.mn_major = mn_major;
     op.tile_mn = tile_mn;
+    op.es = es;
+    op.bk = (int)(kSwizzleSpan / es);
+    op.mma_k = 32 / es;
+    const uint32_t T = kSwizzleSpan / es;             // elements per 128-byte row
     if (!mn_major) {
-        op.box_inner = kBK;              // K, 128 bytes
+        op.box_inner = op.bk;            // K, 128 bytes
         op.box_outer = tile_mn;          // MN rows
         op.nbox = 1;
         op.box_bytes = tile_mn * kSwizzleSpan;
         op.lbo = 16;                     // unused by swizzled K-major layouts
         op.sbo = kSwizzleAtom;           // next group of 8 rows
-        op.kstep = kMmaK * 2;            // 32 bytes along the swizzled row
+        op.kstep = op.mma_k * es;        // 32 bytes along the swizzled row
     } else {
-        op.box_inner = 64;               // MN, 128 bytes
-        op.box_outer = kBK;              // K rows
-        op.nbox = tile_mn / 64;
-        op.box_bytes = kBK * kSwizzleSpan;
-        op.lbo = op.box_bytes;           // next 64-wide MN atom = next box
+        op.box_inner = T;                // MN, 128 bytes
+        op.box_outer = op.bk;            // K rows
+        op.nbox = tile_mn / (int)T;
+        op.box_bytes = op.bk * kSwizzleSpan;
+        op.lbo = op.box_bytes;           // next 128-byte-wide MN atom = next box
         op.sbo = kSwizzleAtom;           // next group of 8 k rows
-        op.kstep = 2 * kSwizzleAtom;     // 16 k rows
+        op.kstep = op.mma_k * kSwizzleSpan;   // mma_k k rows of 128 bytes
     }
     op.stage_bytes = op.box_bytes * op.nbox;
     op.desc_hi = desc_hi(op.lbo, op.sbo);
 
     // ---- F2 model and checks ------------------------------------------------
     op.bits_mn = log2i(tile_mn);
-    op.bits_k = log2i(kBK);
+    op.bits_k = log2i(op.bk);
     for (int i = 0; i < op.bits_mn; ++i) op.basis_mn[i] = tma_offset(op, 1u << i, 0);
     for (int i = 0; i < op.bits_k; ++i) op.basis_k[i] = tma_offset(op, 0, 1u << i);
     bool linear = true, same = true;
-    std::vector<uint8_t> hit(op.stage_bytes / 2, 0);
-    bool inj = true;
+    std::vector<uint8_t> hit(op.nbox > 0 ? op.stage_bytes / es : 0, 0);
+    bool inj = op.nbox > 0;
     for (uint32_t mn = 0; mn < (uint32_t)tile_mn; ++mn) {
-        for (uint32_t k = 0; k < (uint32_t)kBK; ++k) {
+        for (uint32_t k = 0; k < (uint32_t)op.bk; ++k) {
             uint32_t t = tma_offset(op, mn, k);
             uint32_t x = 0;
             for (int i = 0; i < op.bits_mn; ++i) if ((mn >> i) & 1) x ^= op.basis_mn[i];
             for (int i = 0; i < op.bits_k; ++i) if ((k >> i) & 1) x ^= op.basis_k[i];
             linear &= (x == t);
             same &= (umma_offset(op, mn, k) == t);
-            if (t / 2 >= hit.size() || hit[t / 2]) inj = false; else hit[t / 2] = 1;
+            if (t / es >= hit.size() || hit[t / es]) inj = false; else hit[t / es] = 1;
         }
     }
     op.linear = linear;
     op.tma_equals_umma = same;
     op.bijective = inj && std::all_of(hit.begin(), hit.end(), [](uint8_t h) { return h != 0; });
-    // Left division by the 16-byte contiguous row of a core matrix: the first
-    // three bases of the contiguous dimension must be 2, 4, 8 bytes and every
+    // Left division by the 16-byte contiguous row of a core matrix: the bases
+    // of the contiguous dimension must be es, 2 es, ..., 8 bytes and every
     // other basis a multiple of 16 bytes.
     const uint32_t* cont = op.mn_major ? op.basis_mn : op.basis_k;
     int ncont = op.mn_major ? op.bits_mn : op.bits_k;
-    bool div = ncont >= 3 && cont[0] == 2 && cont[1] == 4 && cont[2] == 8;
-    for (int i = 3; i < ncont; ++i) div &= (cont[i] % 16) == 0;
+    const int inner = log2i(16u / (uint32_t)es);      // bases inside one 16-byte row
+    bool div = ncont >= inner;
+    for (int i = 0; i < inner && i < ncont; ++i) div &= cont[i] == ((uint32_t)es << i);
+    for (int i = inner; i < ncont; ++i) div &= (cont[i] % 16) == 0;
     const uint32_t* other = op.mn_major ? op.basis_k : op.basis_mn;
     int nother = op.mn_major ? op.bits_k : op.bits_mn;
     for (int i = 0; i < nother; ++i) div &= (other[i] % 16) == 0;
@@ -138,7 +148,8 @@ int bank_degree_16B(const uint32_t* addr, int lanes) {
 }  // namespace
 
 uint32_t make_idesc(int in_dtype, int a_mn_major, int b_mn_major, int M, int N) {
-    uint32_t fmt = (in_dtype == 0) ? 1u : 0u;     // BF16 = 1, F16 = 0
+    // A / B format field: kind::f16 F16 = 0, BF16 = 1; kind::f8f6f4 E4M3 = 0, E5M2 = 1
+    uint32_t fmt = (in_dtype == 0 || in_dtype == 4) ? 1u : 0u;
     uint32_t d = 0;
     d |= 1u << 4;                                  // D format: F32
     d |= fmt << 7;                                 // A format
@@ -160,7 +171,15 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
         p.why = "dimension beyond 2^31-1";
         return p;
     }
-    p.num_k = (int)((K + kBK - 1) / kBK);
+    if (in_dtype != 0 && in_dtype != 1 && in_dtype != 3 && in_dtype != 4) {
+        p.why = "input type";
+        return p;
+    }
+    p.in_es = (in_dtype == 3 || in_dtype == 4) ? 1 : 2;
+    p.kind = p.in_es == 1 ? 1 : 0;
+    p.bk = (int)(kSwizzleSpan / p.in_es);
+    p.mma_k = 32 / p.in_es;
+    p.num_k = (int)((K + p.bk - 1) / p.bk);
     auto tiles_for = [&](int tm, int bn) { return ((M + tm - 1) / tm) * ((N + bn - 1) / bn) * batch; };
     // Wave quantisation, in units of one 128 x 256 tile on one SM: a 128-wide
     // tile costs a bit over half of that; a CTA pair computes a 256 x 256 tile
@@ -186,8 +205,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.idesc = make_idesc(in_dtype, a_major, b_major, p.tile_m, bn);
 
     // Per-CTA operand tiles: A 128 rows; B all BN columns, or half of them in a pair.
-    plan_operand(p.a, a_major, kBM);
-    plan_operand(p.b, b_major, p.pair ? bn / 2 : bn);
+    plan_operand(p.a, a_major, kBM, p.in_es);
+    plan_operand(p.b, b_major, p.pair ? bn / 2 : bn, p.in_es);
 
     p.c.out_es = (out_dtype == 2) ? 4 : 2;
     p.c.chunk_cols = 128 / p.c.out_es;
@@ -261,12 +280,13 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->total_tiles = p.tiles;
     kp->BN = p.BN; kp->stages = p.stages;
     kp->kgroup = p.kgroup;
+    kp->bk = p.bk;
     kp->idesc = p.idesc;
     kp->a_mn_major = p.a.mn_major; kp->b_mn_major = p.b.mn_major;
     kp->a_nbox = p.a.nbox; kp->b_nbox = p.b.nbox;
     kp->a_box_bytes = p.a.box_bytes; kp->b_box_bytes = p.b.box_bytes;
-    kp->a_box_mn = p.a.mn_major ? 64 : p.a.box_outer;
-    kp->b_box_mn = p.b.mn_major ? 64 : p.b.box_outer;
+    kp->a_box_mn = p.a.mn_major ? p.a.box_inner : p.a.box_outer;
+    kp->b_box_mn = p.b.mn_major ? p.b.box_inner : p.b.box_outer;
     kp->a_kstep = p.a.kstep; kp->b_kstep = p.b.kstep;
     kp->a_desc_hi = p.a.desc_hi; kp->b_desc_hi = p.b.desc_hi;
     kp->stage_stride = p.stage_stride;
@@ -297,7 +317,7 @@ std::string describe_json(const Plan& p) {
     };
     o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
       << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
-      << ",\"pair\":" << p.pair << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << kBK << ",\"mma_k\":" << kMmaK
+      << ",\"pair\":" << p.pair << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
       << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads

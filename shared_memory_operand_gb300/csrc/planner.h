@@ -21,6 +21,9 @@ namespace smo {
 struct OperandPlan {
     int mn_major = 0;
     int tile_mn = 0;                // rows of the operand tile in its MN dimension
+    int es = 2;                     // bytes per element (2: bf16 / f16, 1: FP8)
+    int bk = 64;                    // K per stage: one 128-byte swizzle row of K-major elements
+    int mma_k = 16;                 // K per tcgen05.mma: 32 bytes of K
     uint32_t box_inner = 0, box_outer = 0;   // TMA box (elements)
     int nbox = 0;
     uint32_t box_bytes = 0, stage_bytes = 0;
@@ -44,6 +47,9 @@ struct EpiPlan {
 struct Plan {
     int64_t M = 0, N = 0, K = 0, batch = 1;
     int in_dtype = 0, out_dtype = 0;
+    int in_es = 2;                  // input element bytes
+    int bk = 64, mma_k = 16;        // K per stage / per MMA (128 / in_es, 32 / in_es)
+    int kind = 0;                   // tcgen05.mma kind: 0 kind::f16, 1 kind::f8f6f4
     int pair = 0;                   // 1: CTA pair (cta_group::2), 256 x BN tiles over two SMs
     int tile_m = 128;               // output rows per tile (128, or 256 for a pair)
     int BN = 256, stages = 4;
@@ -59,7 +65,8 @@ struct Plan {
     std::string why;                // reason when !ok
 };
 
-// in_dtype: 0 bf16, 1 f16.  out_dtype: 0 bf16, 1 f16, 2 f32 (gemm_dtype_t).
+// in_dtype: 0 bf16, 1 f16, 3 FP8 E4M3, 4 FP8 E5M2.  out_dtype: 0 bf16, 1 f16,
+// 2 f32 (gemm_dtype_t).
 // force: 0 = choose; 128 or 256 = one CTA with that BN; 512 = CTA pair (256 x 256).
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
                int out_dtype, int64_t batch, int num_sms, int force);

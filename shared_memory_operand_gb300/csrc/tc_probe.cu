@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(128, 1)
         for (int i = 0; i < iters; ++i) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                smo::umma_f16_pair(tmem, a_desc + (uint64_t)(k * 2), b_desc + (uint64_t)(k * 2), idesc, (i | k) != 0);
+                smo::umma_pair<smo::KIND_F16>(tmem, a_desc + (uint64_t)(k * 2), b_desc + (uint64_t)(k * 2), idesc, (i | k) != 0);
         }
         smo::umma_commit_pair_mc(bar, (uint16_t)(1u << lead));
         const bool ok = smo::mbar_wait(bar, 0, budget_ns);

@@ -64,8 +64,8 @@ def oracle_full(p):
 
 
 def scale(p) -> float:
-    a = p.logical_A().abs().max().item() if p.M * p.K else 0.0
-    b = p.logical_B().abs().max().item() if p.K * p.N else 0.0
+    a = p.logical_A().to(torch.float32).abs().max().item() if p.M * p.K else 0.0
+    b = p.logical_B().to(torch.float32).abs().max().item() if p.K * p.N else 0.0
     return max(a * b, 1e-30)
 
 

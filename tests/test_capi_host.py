@@ -66,9 +66,14 @@ def test_argument_validation_without_device(lib):
     assert _ex(batch=2, sa=64 * 64, sb=64 * 64, sc=64) == smo.GEMM_ERR_ARG   # C batches overlap
     assert _ex(batch=2, sa=4100, sb=4096, sc=4096) == smo.GEMM_ERR_ALIGN
     assert _ex(M=1 << 31) == smo.GEMM_ERR_UNSUPPORTED
+    assert _ex(i=5) == smo.GEMM_ERR_UNSUPPORTED        # no such input type
+    # FP8 operands: one byte per element, so pitches need 16 elements
+    assert _ex(i=3, lda=72, K=66) == smo.GEMM_ERR_ALIGN
+    assert _ex(i=4, lda=80, bm=0, ldb=72, K=66) == smo.GEMM_ERR_ALIGN
     # well-formed arguments reach the device query: no GPU here
     if not _have_gpu():
         assert _ex() == smo.GEMM_ERR_NO_DEVICE
+        assert _ex(i=3, lda=80, K=66) == smo.GEMM_ERR_NO_DEVICE
         assert smo.gemm_check(0) == smo.GEMM_ERR_NO_DEVICE
 
 
@@ -118,6 +123,39 @@ def test_planner_layouts_match_oracle(lib, am, bm, out):
             assert op["stage_bytes"] == tile * 64 * 2
 
 
+@pytest.mark.parametrize("am", [0, 1])
+@pytest.mark.parametrize("bm", [0, 1])
+@pytest.mark.parametrize("ind", ["e4m3", "e5m2"])
+def test_planner_fp8_layouts_match_oracle(lib, am, bm, ind):
+    """One-byte operands: a stage is 128 K values (one 128-byte swizzle row), an
+    MMA takes 32, and an MN-major box is 128 MN values wide; the planner's F2
+    bases and descriptor strides reproduce the oracle's layouts exactly."""
+    for (M, N, K) in SHAPES:
+        d = smo.gemm_plan_describe(M, N, K, am, bm, ind, "bf16")
+        assert d["ok"], d["why"]
+        assert d["BK"] == 128 and d["mma_k"] == 32 and d["kind"] == 1 and d["in_es"] == 1
+        assert d["smem_bytes"] <= 232448
+        for name, major in (("A", am), ("B", bm)):
+            op = d[name]
+            tile = op["tile_mn"]
+            mn_major = bool(major)
+            want_mn = [banksim.operand_tile_offset(1 << i, 0, mn_major, tile, elem_bytes=1, box_k=128)
+                       for i in range(tile.bit_length() - 1)]
+            want_k = [banksim.operand_tile_offset(0, 1 << i, mn_major, tile, elem_bytes=1, box_k=128)
+                      for i in range(7)]
+            assert op["basis_mn"] == want_mn
+            assert op["basis_k"] == want_k
+            for mn in range(0, tile, 5):
+                for k in range(128):
+                    assert banksim.umma_canonical_offset(mn, k, mn_major, op["lbo"], op["sbo"],
+                                                         op["kstep_bytes"], elem_bytes=1, mma_k=32) == \
+                        banksim.operand_tile_offset(mn, k, mn_major, tile, elem_bytes=1, box_k=128)
+            assert op["linear"] and op["bijective"] and op["tma_equals_umma"]
+            assert op["core_matrix_divides"]
+            assert op["stage_bytes"] == tile * 128
+            assert op["box"] == ([128, tile] if not mn_major else [128, 128])
+
+
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_epilogue_stores_conflict_free(lib, out):
     d = smo.gemm_plan_describe(1024, 1024, 1024, 0, 1, "bf16", out)
@@ -154,6 +192,21 @@ def test_instruction_descriptor_fields(lib):
                 assert ((x >> 17) & 63) * 8 == d["BN"]
                 assert ((x >> 24) & 31) * 16 == d["BM"]
                 assert x & 0b1111 == 0 and (x >> 13) & 3 == 0 and (x >> 23) & 1 == 0
+
+
+def test_instruction_descriptor_fp8_fields(lib):
+    """kind::f8f6f4 instruction descriptor: A / B format E4M3 = 0, E5M2 = 1 in
+    bits 7-9 / 10-12, the other fields as for kind::f16."""
+    for am in (0, 1):
+        for bm in (0, 1):
+            for ind, fmt in (("e4m3", 0), ("e5m2", 1)):
+                d = smo.gemm_plan_describe(4096, 4096, 4096, am, bm, ind, "bf16")
+                x = d["idesc"]
+                assert (x >> 4) & 3 == 1
+                assert (x >> 7) & 7 == fmt and (x >> 10) & 7 == fmt
+                assert (x >> 15) & 1 == am and (x >> 16) & 1 == bm
+                assert ((x >> 17) & 63) * 8 == d["BN"] and ((x >> 24) & 31) * 16 == d["BM"]
+                assert d["num_k"] == 4096 // 128
 
 
 def test_tile_choice_and_grid(lib):

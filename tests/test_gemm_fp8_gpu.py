@@ -1,0 +1,127 @@
+"""GPU parity of the 8-bit operand path (tcgen05.mma.kind::f8f6f4) against the
+fp64 oracle, through the C ABI.
+
+FP8 values multiply exactly and the tensor core accumulates in fp32, so the
+tolerances are those of the 16-bit path (tests/gemm_check.py), and integer
+inputs must match bit for bit.  The operands are E4M3 / E5M2 codes of the OCP
+8-bit format ("An Educational GEMM Ladder for Helios GPUs": FP8 matrix units;
+"A Deep Dive into LDS Optimizations on AMD Instinct MI450 GPUs", Part I: the
+8-bit transposed load, whose GB300 counterpart is the MN-major descriptor).
+"""
+import numpy as np
+import pytest
+import torch
+
+import shared_memory_operand_gb300 as smo
+from synthetic import K_MAJOR, MN_MAJOR, make_problem, workload
+from tests.gemm_check import check, oracle_full, oracle_sampled, run_gpu, sample_positions
+
+pytestmark = pytest.mark.gpu
+
+MAJORS = [(K_MAJOR, K_MAJOR), (K_MAJOR, MN_MAJOR), (MN_MAJOR, K_MAJOR), (MN_MAJOR, MN_MAJOR)]
+FP8 = ["e4m3", "e5m2"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    smo.load_library(build=True)
+    yield
+
+
+def _full(p, exact=False):
+    return check(p, run_gpu(p), oracle_full(p), exact=exact)
+
+
+@pytest.mark.parametrize("am,bm", MAJORS)
+@pytest.mark.parametrize("dt", FP8)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_small_ragged_all_orientations(am, bm, dt, out):
+    # K = 65 / 200: one partial 128-deep stage; 129 x 257: ragged M and N
+    for (M, N, K) in [(256, 256, 128), (300, 520, 200), (129, 257, 65), (1, 16, 32), (192, 384, 384)]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype=dt, out_dtype=out, dist="uniform",
+                         seed=M + N + K)
+        _full(p)
+
+
+@pytest.mark.parametrize("mode", [128, 256, 512])
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_tile_modes_ragged(monkeypatch, mode, am, bm):
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", str(mode))
+    # (384, 640): MN extents multiples of 128 (one-instruction 4-D loads of
+    # MN-major FP8 operands) but not of the tile
+    for (M, N, K, out) in [(600, 700, 300, "bf16"), (257, 513, 129, "f32"), (384, 640, 256, "f32"),
+                           (520, 1030, 1000, "f16")]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="e4m3", out_dtype=out,
+                         dist="uniform", seed=M + K + mode)
+        _full(p)
+
+
+@pytest.mark.parametrize("am,bm", MAJORS)
+@pytest.mark.parametrize("dt", FP8)
+def test_integer_inputs_bit_exact(am, bm, dt):
+    """Integers in [-4, 4] are exact in both formats and every partial sum
+    (|s| <= 16 K) is exact in fp32."""
+    for (M, N, K) in [(200, 300, 1000), (256, 512, 4096)]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype=dt, out_dtype="f32", dist="int",
+                         seed=3 + K)
+        _full(p, exact=True)
+
+
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_permutation_operands_exact(am, bm):
+    """A = permutation matrix: every output is one B element, moved; a wrong
+    descriptor stride or major bit shows up as a moved row or column."""
+    g = torch.Generator().manual_seed(21)
+    K, N = 256, 384
+    perm = torch.randperm(K, generator=g)
+    p = make_problem(K, N, K, a_major=am, b_major=bm, in_dtype="e4m3", out_dtype="f32", dist="uniform",
+                     seed=5)
+    p.logical_A()[0].copy_(torch.eye(K)[perm].to(torch.float8_e4m3fn))
+    gpu = run_gpu(p)
+    want = p.logical_B()[0].to(torch.float64).numpy()[perm.numpy()]
+    assert np.array_equal(gpu[0], want)
+
+
+def test_batched_and_k_tails():
+    for K in (1, 16, 127, 129, 383):
+        p = make_problem(130, 260, K, in_dtype="e5m2", out_dtype="bf16", dist="uniform", seed=K, batch=3)
+        _full(p)
+
+
+def test_stream_k_full_compare(monkeypatch):
+    """Stream-K on the CTA pair with FP8 stages (128 K per block)."""
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
+    p = make_problem(1536, 2560, 4096, in_dtype="e4m3", out_dtype="f32", dist="uniform", seed=77)
+    _full(p)
+    q = make_problem(1536, 2560, 4096, in_dtype="e4m3", out_dtype="f32", dist="int", seed=78)
+    _full(q, exact=True)
+
+
+def test_alignment_rule_for_one_byte_elements():
+    """FP8 leading dimensions must be multiples of 16 elements (16 bytes)."""
+    A = torch.zeros(64 * 72, dtype=torch.uint8, device="cuda")
+    B = torch.zeros(64 * 64, dtype=torch.uint8, device="cuda")
+    C = torch.zeros(64 * 64, dtype=torch.float32, device="cuda")
+    st = smo.gemm_ex_status(A, 72, 0, B, 64, 0, C, 64, 64, 64, 64, in_dtype="e4m3", out_dtype="f32")
+    assert st == smo.GEMM_ERR_ALIGN
+    st = smo.gemm_ex_status(A, 80, 0, B, 64, 0, C, 64, 64, 64, 64, in_dtype="e4m3", out_dtype="f32")
+    assert st == smo.GEMM_OK
+    assert smo.gemm_check(None) == smo.GEMM_OK
+
+
+@pytest.mark.parametrize("name", ["gemm_8192_e4m3_bf16_AK_BN", "gemm_8192_e4m3_bf16_AK_BK"])
+def test_config_8192_fp8(name):
+    p = workload(name)
+    gpu = run_gpu(p)
+    bi, mi, ni = sample_positions(p, 2000)
+    check(p, gpu[bi, mi, ni], oracle_sampled(p, bi, mi, ni))
+    assert np.all(np.isfinite(gpu))
+
+
+def test_config_8192_fp8_integer_bit_exact():
+    p = workload("gemm_8192_e4m3_bf16_AK_BN", dist="int", out_dtype="f32")
+    gpu = run_gpu(p)
+    bi, mi, ni = sample_positions(p, 3000)
+    check(p, gpu[bi, mi, ni], oracle_sampled(p, bi, mi, ni), exact=True)
