@@ -227,12 +227,13 @@ def run_reference(args, world, rank):
     value = flops * args.steps / dt / 1e12
     sample = f"first {rows} of {p.M} rows of the {args.workload} product (full N={p.N}, K={p.K}) per step"
     line = {
-        "impl": "reference", "metric": "BF16 GEMM TFLOP/s", "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": "FP8 GEMM TFLOP/s" if p.in_dtype in ("e4m3", "e5m2") else "BF16 GEMM TFLOP/s",
+        "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "M": p.M, "N": p.N, "K": p.K,
-                   "a_major": "K", "b_major": "N" if p.b_major else "K",
+                   "a_major": "M" if p.a_major else "K", "b_major": "N" if p.b_major else "K",
                    "in": p.in_dtype, "out": p.out_dtype, "sample_rows": rows},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -297,7 +298,7 @@ def run_ours(args, world, rank, local):
     # Inputs + output larger than twice the 129 MB L2 stream from HBM anyway;
     # smaller working sets get L2 flushed (256 MiB written) before every launch,
     # outside the per-launch event pair.
-    work_bytes = (p.A.numel() + p.B.numel()) * 2 + C.numel() * C.element_size()
+    work_bytes = (p.A.numel() + p.B.numel()) * p.A.element_size() + C.numel() * C.element_size()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if work_bytes < (258 << 20) else None
     def timing_event():
         # events recorded inside a CUDA graph need the "external" record flag to be timed
@@ -415,11 +416,18 @@ def run_ours(args, world, rank, local):
     achieved = p.flops / avg_launch_s / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    alg_bytes = (p.M * p.K + p.K * p.N) * 2 * p.batch + p.M * p.N * C.element_size() * p.batch
+    peak_note = f"bf16_tflops (burst) of {peak_src}"
+    fp8 = p.in_dtype in ("e4m3", "e5m2")
+    if fp8:
+        # the measured peak is a bf16 GEMM's; FP8 takes it times the nominal
+        # dense FP8 / BF16 tensor ratio (4.5 / 2.25 PFLOP/s)
+        peak, peak_sus = 2.0 * peak, 2.0 * peak_sus
+        peak_note += " x 2 (nominal dense FP8 / BF16 ratio 4.5 / 2.25)"
+    alg_bytes = (p.M * p.K + p.K * p.N) * p.A.element_size() * p.batch + p.M * p.N * C.element_size() * p.batch
     traffic = profiled_traffic(args.workload)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"bf16_tflops (burst) of {peak_src}",
+                "peak_source": peak_note,
                 "frac_of_sustained": achieved / peak_sus, "algorithmic_bytes": alg_bytes,
                 "kernel": KERNEL_NAME, "launch_ms_median": statistics.median(launch_ms)}
 
@@ -435,10 +443,10 @@ def run_ours(args, world, rank, local):
                    "sample": str(e)}
 
     line = {
-        "metric": "BF16 GEMM TFLOP/s", "value": agg["value"], "unit": "TFLOP/s",
+        "metric": "FP8 GEMM TFLOP/s" if fp8 else "BF16 GEMM TFLOP/s", "value": agg["value"], "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": agg["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": p.in_dtype, "data": "synthetic",
         "config": {"workload": args.workload, "M": p.M, "N": p.N, "K": p.K, "batch": p.batch,
                    "a_major": "M" if p.a_major else "K", "b_major": "N" if p.b_major else "K",
                    "in": p.in_dtype, "accumulate": "f32", "out": p.out_dtype,
@@ -447,7 +455,8 @@ def run_ours(args, world, rank, local):
                           "pairs; steps timed by those pairs)") if flush is not None else
                          "no flush: A+B+C larger than twice the 129 MB L2",
                    "launch": "cuda graph replay" if args.graph else "back-to-back host launches",
-                   "pct_of_dense_bf16_peak": 100.0 * agg["value"] / world / peak},
+                   ("pct_of_dense_fp8_peak" if fp8 else "pct_of_dense_bf16_peak"):
+                       100.0 * agg["value"] / world / peak},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
