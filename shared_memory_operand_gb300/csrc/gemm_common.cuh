@@ -43,7 +43,7 @@ struct LoadSlot {
     uint32_t dst_off;      // from the stage base
     uint32_t mode;         // 0 fused, 1 K-major box, 2 MN-major box
     int32_t mn_off;        // offset of this box along MN
-    int32_t box_mn;        // MN extent of one box
+    int32_t box_mn_log2;   // log2 of the MN extent of one box (64 or 128 elements, or a tile's rows)
     bool is_a;
 };
 
@@ -62,8 +62,9 @@ __device__ __forceinline__ LoadSlot load_slot(const KParams& p, const CUtensorMa
     s.tm = s.is_a ? tmA : tmB;
     s.dst_off = (s.is_a ? 0u : p.b_off) + j * (s.is_a ? p.a_box_bytes : p.b_box_bytes);
     s.mode = fused ? 0u : (mn_major ? 2u : 1u);
-    s.box_mn = (int32_t)(s.is_a ? p.a_box_mn : p.b_box_mn);
-    s.mn_off = (int32_t)j * s.box_mn;
+    const uint32_t box_mn = s.is_a ? p.a_box_mn : p.b_box_mn;   // a power of two
+    s.box_mn_log2 = 31 - __clz((int)box_mn);
+    s.mn_off = (int32_t)(j * box_mn);
     return s;
 }
 
@@ -72,7 +73,7 @@ __device__ __forceinline__ LoadSlot load_slot(const KParams& p, const CUtensorMa
 __device__ __forceinline__ void slot_coords(const LoadSlot& s, int32_t mn0, int32_t k0, int32_t& c0, int32_t& c1,
                                             int32_t& c2) {
     if (s.mode == 0) {
-        c0 = 0; c1 = k0; c2 = mn0 / s.box_mn;
+        c0 = 0; c1 = k0; c2 = mn0 >> s.box_mn_log2;
     } else if (s.mode == 1) {
         c0 = k0; c1 = mn0 + s.mn_off; c2 = 0;
     } else {
