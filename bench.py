@@ -480,7 +480,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-check", action="store_true")
+    ap.add_argument("--no-check", action="store_true",
+                    help="accepted for older command lines; the device error word is always checked")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
                     help="replay the timed launches from a CUDA graph (launch-bound shapes)")

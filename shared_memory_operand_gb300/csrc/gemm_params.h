@@ -48,7 +48,7 @@ struct KParams {
     uint32_t a_fused, b_fused;      // 1: an MN-major operand's boxes come from one 4-D TMA load
     uint32_t a_box_bytes, b_box_bytes;
     uint32_t a_box_mn, b_box_mn;    // MN extent of one box
-    uint32_t a_kstep, b_kstep;      // descriptor start-address advance per 16-wide K step (bytes)
+    uint32_t a_kstep, b_kstep;      // descriptor start-address advance per MMA K step (bytes)
     uint64_t a_desc_hi, b_desc_hi;  // smem descriptor fields other than the start address
     uint32_t stage_stride;          // bytes per pipeline stage (A then B)
     uint32_t b_off;                 // offset of B inside a stage
