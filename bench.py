@@ -49,16 +49,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the GEMM kernel's sources (the shared-memory probe excluded)."""
+def _code_only(text: str) -> str:
+    """C / C++ source without comments and with whitespace runs collapsed, so
+    that a comment edit does not count as a kernel change."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(csrc: str = None) -> str:
+    """Hash of the GEMM kernel's code (comments ignored; the probes excluded)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "shared_memory_operand_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "shared_memory_operand_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith("smem_probe") or name.startswith("tc_probe"):
             continue
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
