@@ -34,8 +34,8 @@ struct DevState {
     int num_sms = 0;
     int32_t* d_err = nullptr;
     bool attr_set[12] = {};         // one-CTA kernels: [(KIND * 3 + OUT) * 2 + KG - 1]
-    bool pair_attr_set[6] = {};     // pair kernels: [KIND * 3 + OUT]
-    int pair_max_clusters[3] = {0, 0, 0};   // co-resident 2-CTA clusters of the pair kernel
+    bool pair_attr_set[12] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT]
+    int pair_max_clusters[12] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
     // Stream-K workspace, one per stream so that GEMMs running concurrently
     // on different streams never share partial slots or tile counters.
     struct SkWork {
@@ -95,7 +95,7 @@ int force_bn_from_env() {
     const char* s = std::getenv("SMO_GEMM_FORCE_BN");
     if (!s) return 0;
     int v = std::atoi(s);
-    return (v == 128 || v == 256 || v == 512) ? v : 0;
+    return (v == 128 || v == 256 || v == 512 || v == 1024) ? v : 0;
 }
 
 // Lazily initialises the per-device state of the current device.
@@ -239,10 +239,11 @@ int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUt
 // as many clusters as can be co-resident.  With stream-K the whole tiles are
 // dealt round-robin and the K blocks of the last, partial wave's tiles are
 // shared out evenly, so that every cluster ends at the same time.
-template <int OUT, int KIND>
+template <int OUT, int KIND, int WIDE>
 int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 KParams kp, cudaStream_t stream, int stream_k) {
-    auto kern = smo::smo_gemm_pair_kernel<OUT, KIND>;
+    auto kern = smo::smo_gemm_pair_kernel<OUT, KIND, WIDE>;
+    const int slot = (WIDE * 2 + KIND) * 3 + OUT;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];
@@ -255,7 +256,7 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!ds.pair_attr_set[KIND * 3 + OUT]) {
+    if (!ds.pair_attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
             cudaSuccess) {
             cudaGetLastError();
@@ -267,10 +268,10 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
-        ds.pair_max_clusters[OUT] = n;
-        ds.pair_attr_set[KIND * 3 + OUT] = true;
+        ds.pair_max_clusters[slot] = n;
+        ds.pair_attr_set[slot] = true;
     }
-    const int64_t maxc = ds.pair_max_clusters[OUT];
+    const int64_t maxc = ds.pair_max_clusters[slot];
     int64_t clusters = std::min<int64_t>(pl.tiles, maxc);
     kp.sk_clusters = 0;
     kp.dp_tiles = pl.tiles;
@@ -278,14 +279,15 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     if (stream_k != 0) {
         const int64_t waves = pl.tiles / maxc;
         const int64_t sk_tiles = pl.tiles - waves * maxc;
-        // Each split piece moves a 256 KiB fp32 partial through L2 (about
+        // Each split piece moves a 256 KiB (wide tiles: 512 KiB) fp32 partial through L2 (about
         // 20 MB per launch for 76 clusters); measured on GB300 that costs more
         // than the idle tail it removes unless every cluster's share of the
         // split tiles is long.  Automatic: at least 48 K blocks per cluster.
-        const bool worth = stream_k == 1 || (sk_tiles * (int64_t)pl.num_k) / maxc >= 48;
+        // Wide tiles (512 KiB partials) lost 3.5% at 8192^3: automatic only on 256 x 256 tiles.
+        const bool worth = stream_k == 1 || (!pl.wide && (sk_tiles * (int64_t)pl.num_k) / maxc >= 48);
         // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
         if (worth && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
-            const size_t work_bytes = (size_t)maxc * 2 * smo::kBM * (size_t)pl.BN * sizeof(float);
+            const size_t work_bytes = (size_t)maxc * (size_t)pl.tile_m * (size_t)pl.BN * sizeof(float);
             DevState::SkWork* w = nullptr;
             {
                 std::lock_guard<std::mutex> lk(g_mu);
@@ -344,8 +346,9 @@ no_stream_k:
 template <int OUT, int KIND>
 int launch_kind(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KParams& kp, cudaStream_t stream, int stream_k) {
-    return pl.pair ? launch_pair<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream, stream_k)
-                   : launch_single<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream);
+    if (!pl.pair) return launch_single<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream);
+    return pl.wide ? launch_pair<OUT, KIND, 1>(pl, ds, ta, tb, tc, kp, stream, stream_k)
+                   : launch_pair<OUT, KIND, 0>(pl, ds, ta, tb, tc, kp, stream, stream_k);
 }
 
 template <int OUT>

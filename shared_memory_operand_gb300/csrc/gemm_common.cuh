@@ -199,11 +199,12 @@ __device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float* p
 }
 
 // Stream-K partial piece: this warp's 32 accumulator rows (all BN columns,
-// fp32) go to `dst` in the order above, then the warp announces them on
-// `flag`.  `release` is called once the accumulator has been read.
+// fp32) go to `dst` in the order above; with `announce` the warp then
+// publishes everything it has written on `flag`.  `release` is called once
+// the accumulator region has been read.
 template <typename Release>
 __device__ __forceinline__ void epilogue_partial(const KParams& p, uint32_t tmem_acc, uint32_t lane_field, int lane,
-                                                 float* dst, int32_t* flag, Release release) {
+                                                 float* dst, int32_t* flag, bool announce, Release release) {
     for (int c = 0; c < p.BN / 32; ++c) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_acc + lane_field + (uint32_t)(c * 32), v);
@@ -217,6 +218,7 @@ __device__ __forceinline__ void epilogue_partial(const KParams& p, uint32_t tmem
 #pragma unroll
         for (int i = 0; i < 32; ++i) __stcg(out + i * 32, __uint_as_float(v[i]));
     }
+    if (!announce) return;
     __threadfence();
     __syncwarp();
     if (lane == 0) atomicAdd(flag, 1);

@@ -36,12 +36,23 @@ namespace smo {
 
 static_assert(kStageKBytes / kMmaKBytes == 4, "the issue loop unrolls four MMAs per K block");
 constexpr int kPairGroup = 2;       // stages per full/empty barrier pair (the ring holds 6)
+constexpr uint32_t kHalfABytes = kBM * kStageKBytes;   // 128 A rows of one stage, every layout
 
 // KIND: MmaKind (kind::f16 for 16-bit operands, kind::f8f6f4 for FP8).
-template <int OUT, int KIND>
+// WIDE: 0 -- 256 x 256 tiles, 128 A rows per CTA, two accumulators, stages
+//            handed over in groups of two (6 x 32 KiB);
+//       1 -- 512 x 256 tiles, 256 A rows per CTA (two 128-row halves, each
+//            with its own 256 x 256 MMAs into TMEM columns 0..255 / 256..511),
+//            one accumulator, one stage per barrier pair (4 x 48 KiB).  The B
+//            half-panel of a stage then feeds twice the MMAs: 47 instead of 64
+//            operand bytes per tensor cycle, so the same ring keeps more MMA
+//            work in flight.
+template <int OUT, int KIND, int WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+    constexpr int KG = WIDE ? 1 : kPairGroup;      // stages per full/empty barrier pair
+    constexpr int MSUB = WIDE ? 2 : 1;             // 128-row A halves (and accumulator regions) per CTA
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
@@ -97,8 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((uint32_t)lane < nloads) {
             const uint32_t lmask = (1u << nloads) - 1u;
             const LoadSlot slot = load_slot(p, &tmA, &tmB, (uint32_t)lane);
-            const uint32_t ngroups = (uint32_t)(p.stages / kPairGroup);
-            const uint32_t group_bytes = kPairGroup * p.stage_stride;
+            const uint32_t ngroups = (uint32_t)(p.stages / KG);
+            const uint32_t group_bytes = KG * p.stage_stride;
             uint32_t g = 0, ph = 0, gst = base;           // group index, ring parity, group's smem
             uint32_t issued_mask = 0, issued_ph = 0;
             bool skip_one = p.stall != 0;
@@ -110,10 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int b, mb, nb;
                 decode_tile(p, w.tile, b, mb, nb);
                 // this CTA's A rows / B columns
-                const int32_t mn0 = slot.is_a ? mb * (2 * kBM) + (int32_t)rank * kBM
+                const int32_t mn0 = slot.is_a ? mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM)
                                               : nb * p.BN + (int32_t)rank * half_bn;
-                for (int kb = w.kb0; kb < w.kb1; kb += kPairGroup) {
-                    const bool two = kb + 1 < w.kb1;           // a range's last group may hold one block
+                for (int kb = w.kb0; kb < w.kb1; kb += KG) {
+                    const bool two = KG == 2 && kb + 1 < w.kb1;   // a range's last group may hold one block
                     int good = 1;
                     if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
@@ -152,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && rank == 0) {
                 // Every armed group has received both CTAs' bytes (immediate when
                 // the MMA thread already consumed it).
-                for (uint32_t q = 0; q < (uint32_t)(p.stages / kPairGroup); ++q) {
+                for (uint32_t q = 0; q < (uint32_t)(p.stages / KG); ++q) {
                     if ((issued_mask >> q) & 1u) {
                         if (!mbar_wait(full_bar(q), (issued_ph >> q) & 1u, budget))
                             report_error(p.err, DEV_TIMEOUT_TEARDOWN);
@@ -173,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Everything the issue loop needs sits in registers: the single
             // issuing thread, not the tensor pipe, is the limit when each K
             // block's MMAs wait behind parameter loads and address arithmetic.
-            const uint32_t ngroups = (uint32_t)(p.stages / kPairGroup);
+            const uint32_t ngroups = (uint32_t)(p.stages / KG);
             const uint64_t stage_desc = p.stage_stride >> 4;                // descriptor units per stage
-            const uint64_t group_desc = kPairGroup * stage_desc;
+            const uint64_t group_desc = KG * stage_desc;
             const uint64_t a_desc0 = p.a_desc_hi | (uint64_t)((base >> 4) & 0x3FFFu);
             const uint64_t b_desc0 = p.b_desc_hi | (uint64_t)(((base + p.b_off) >> 4) & 0x3FFFu);
             const uint64_t ak = p.a_kstep >> 4, bk = p.b_kstep >> 4;
@@ -188,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             WorkItem w;
             work_begin(p, cluster_id, nclusters, wi);
             for (; ok && work_next(p, wi, w); ++it) {
-                const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+                // two accumulators alternate; a wide tile fills all 512 columns
+                const uint32_t buf = WIDE ? 0u : (it & 1u), aph = WIDE ? (it & 1u) : ((it >> 1) & 1u);
                 if (!mbar_wait(acce_bar(buf), aph ^ 1u, budget)) {
                     report_error(p.err, DEV_TIMEOUT_MMA);
                     ok = false;
@@ -196,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = w.kb0; kb < w.kb1; kb += kPairGroup) {
+                for (int kb = w.kb0; kb < w.kb1; kb += KG) {
                     if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
@@ -204,11 +216,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
-                    umma_pair<KIND>(d_tmem, ad, bd, idesc, (uint32_t)(kb != w.kb0));
+                    const uint32_t acc0 = (uint32_t)(kb != w.kb0);
+                    umma_pair<KIND>(d_tmem, ad, bd, idesc, acc0);
                     umma_pair<KIND>(d_tmem, ad + ak, bd + bk, idesc, 1u);
                     umma_pair<KIND>(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
                     umma_pair<KIND>(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
-                    if (kb + 1 < w.kb1) {
+                    if (WIDE) {
+                        // second 128-row half of A (16 KiB further in every layout)
+                        // into accumulator columns 256..511
+                        const uint64_t ah = ad + (kHalfABytes >> 4);
+                        const uint32_t d1 = d_tmem + 256u;
+                        umma_pair<KIND>(d1, ah, bd, idesc, acc0);
+                        umma_pair<KIND>(d1, ah + ak, bd + bk, idesc, 1u);
+                        umma_pair<KIND>(d1, ah + 2 * ak, bd + 2 * bk, idesc, 1u);
+                        umma_pair<KIND>(d1, ah + 3 * ak, bd + 3 * bk, idesc, 1u);
+                    } else if (kb + 1 < w.kb1) {
                         ad += stage_desc;
                         bd += stage_desc;
                         umma_pair<KIND>(d_tmem, ad, bd, idesc, 1u);
@@ -240,13 +262,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         WorkIter wi;
         WorkItem w;
         work_begin(p, cluster_id, nclusters, wi);
-        const int64_t slot_floats = 2 * kBM * (int64_t)p.BN;          // one cluster's partial slot
-        // this warp's region of a slot: 32 rows x BN fp32
-        const int64_t warp_rows = ((int64_t)rank * kEpiWarps + (int64_t)q) * kEpiRowsPerWarp * p.BN;
+        const int64_t slot_floats = 2 * MSUB * kBM * (int64_t)p.BN;   // one cluster's partial slot
+        // this warp's share of accumulator region i in a slot: 32 rows x BN fp32
+        auto warp_rows = [&](int i) {
+            return (((int64_t)rank * MSUB + i) * kEpiWarps + (int64_t)q) * kEpiRowsPerWarp * p.BN;
+        };
         for (; work_next(p, wi, w); ++it) {
             int b, mb, nb;
             decode_tile(p, w.tile, b, mb, nb);
-            const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+            const uint32_t buf = WIDE ? 0u : (it & 1u), aph = WIDE ? (it & 1u) : ((it >> 1) & 1u);
             int good = 1;
             if (lane == 0) good = mbar_wait(accf_bar(buf), aph, budget) ? 1 : 0;
             good = __shfl_sync(0xffffffffu, good, 0);
@@ -259,8 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc = tmem_base + buf * (uint32_t)p.BN;
             if (w.role == ROLE_PARTIAL) {
                 // later K blocks of a stream-K tile: publish the fp32 partial
-                epilogue_partial(p, acc, lane_field, lane, p.sk_work + cluster_id * slot_floats + warp_rows,
-                                 p.sk_flags + w.sk_tile, [&] { mbar_arrive_cluster(acce); });
+                // (the warp announces it once, after its last region)
+                for (int i = 0; i < MSUB; ++i) {
+                    epilogue_partial(p, acc + (uint32_t)(i * 256), lane_field, lane,
+                                     p.sk_work + cluster_id * slot_floats + warp_rows(i), p.sk_flags + w.sk_tile,
+                                     i == MSUB - 1, [&] {
+                                         if (i == MSUB - 1) mbar_arrive_cluster(acce);
+                                     });
+                }
                 continue;
             }
             uint32_t mask = 0;
@@ -292,12 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (void)ld_acquire_gpu(p.sk_flags + w.sk_tile);    // every lane acquires
                 }
             }
-            const int32_t m0 = mb * (2 * kBM) + (int32_t)rank * kBM + (int32_t)q * kEpiRowsPerWarp;
             const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
-            epilogue_tile<OUT>(p, &tmC, acc, lane_field, slabs, sbuf, lane, m0, nb * p.BN, b,
-                               [&] { mbar_arrive_cluster(acce); },
-                               mask ? p.sk_work + (cluster_id + 1) * slot_floats + warp_rows : nullptr,
-                               slot_floats, mask);
+            for (int i = 0; i < MSUB; ++i) {
+                // CTA `rank`'s accumulator region i holds tile rows rank * 128 * MSUB + i * 128 ...
+                const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
+                                   (int32_t)q * kEpiRowsPerWarp;
+                epilogue_tile<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs, sbuf, lane, m0, nb * p.BN,
+                                   b, [&] {
+                                       if (i == MSUB - 1) mbar_arrive_cluster(acce);
+                                   },
+                                   mask ? p.sk_work + (cluster_id + 1) * slot_floats + warp_rows(i) : nullptr,
+                                   slot_floats, mask);
+            }
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();

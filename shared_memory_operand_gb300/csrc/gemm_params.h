@@ -42,6 +42,7 @@ struct KParams {
     int32_t BN, stages;
     int32_t kgroup;                 // K blocks (stages) per full/empty barrier pair: 1 or 2
     int32_t bk;                     // K elements per stage (128 / input element bytes)
+    int32_t m_sub;                  // 128-row accumulator regions per CTA (2 in a wide CTA pair)
     uint32_t idesc;                 // tcgen05 instruction descriptor
     uint32_t a_mn_major, b_mn_major;
     uint32_t a_nbox, b_nbox;        // TMA boxes per stage and operand

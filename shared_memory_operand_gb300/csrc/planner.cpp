@@ -186,15 +186,24 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     // on two SMs in about 0.85 of it (half the B bytes per SM, deeper pipeline).
     const int64_t clusters = std::max(1, p.num_sms / 2);
     const int64_t t256 = tiles_for(kBM, 256), t128 = tiles_for(kBM, 128), tpair = tiles_for(2 * kBM, 256);
+    const int64_t twide = tiles_for(4 * kBM, 256);
     const double c256 = (double)((t256 + p.num_sms - 1) / p.num_sms) * 1.0;
     const double c128 = (double)((t128 + p.num_sms - 1) / p.num_sms) * 0.55;
     const double cpair = (double)((tpair + clusters - 1) / clusters) * 0.85;
+    // A wide pair tile is two pair tiles' work on three quarters of the
+    // operand bytes (measured about 5% cheaper per flop at 8192^3), but its
+    // single accumulator leaves the epilogue exposed once per tile: it only
+    // wins when every tile runs a long K loop (measured: -19% at 16 K blocks,
+    // -6% at 32, +5% at 64, +7% at 128).
+    const double cwide = (double)((twide + clusters - 1) / clusters) * 1.62;
+    const bool long_k = p.num_k >= 48;
     int choice;
-    if (force == 128 || force == 256 || force == 512) choice = force;
-    else if (cpair <= c256 && cpair <= c128) choice = 512;
+    if (force == 128 || force == 256 || force == 512 || force == 1024) choice = force;
+    else if (cpair <= c256 && cpair <= c128) choice = (long_k && cwide < cpair) ? 1024 : 512;
     else choice = (c128 < c256) ? 128 : 256;
-    p.pair = choice == 512;
-    p.tile_m = p.pair ? 2 * kBM : kBM;
+    p.pair = choice == 512 || choice == 1024;
+    p.wide = choice == 1024;
+    p.tile_m = p.wide ? 4 * kBM : p.pair ? 2 * kBM : kBM;
     const int bn = p.pair ? 256 : choice;
     p.BN = bn;
     p.num_m = (int)((M + p.tile_m - 1) / p.tile_m);
@@ -202,10 +211,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.tiles = tiles_for(p.tile_m, bn);
     p.grid = p.pair ? (int)(2 * std::min<int64_t>(p.tiles, clusters)) : (int)std::min<int64_t>(p.tiles, p.num_sms);
     p.group_m = std::min(p.pair ? 8 : 16, p.num_m);
-    p.idesc = make_idesc(in_dtype, a_major, b_major, p.tile_m, bn);
+    p.idesc = make_idesc(in_dtype, a_major, b_major, p.pair ? 2 * kBM : kBM, bn);
 
-    // Per-CTA operand tiles: A 128 rows; B all BN columns, or half of them in a pair.
-    plan_operand(p.a, a_major, kBM, p.in_es);
+    // Per-CTA operand tiles: A 128 rows (256 in a wide pair); B all BN columns,
+    // or half of them in a pair.
+    plan_operand(p.a, a_major, p.wide ? 2 * kBM : kBM, p.in_es);
     plan_operand(p.b, b_major, p.pair ? bn / 2 : bn, p.in_es);
 
     p.c.out_es = (out_dtype == 2) ? 4 : 2;
@@ -251,11 +261,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     // one-CTA ring would have too few groups in flight to hide the load
     // latency; the CTA-pair kernel (32 KiB stages, six of them) always
     // groups two.
-    if (p.pair && stages < 4) {
+    if (p.pair && !p.wide && stages < 4) {
         p.why = "shared memory too small for two groups of two stages";
         return p;
     }
-    p.kgroup = (p.pair || stages >= 6) ? 2 : 1;
+    if (p.wide && stages < 3) {
+        p.why = "shared memory too small for three wide stages";
+        return p;
+    }
+    // A wide pair's stage already holds 8 MMAs (two 128-row halves of A).
+    p.kgroup = p.wide ? 1 : (p.pair || stages >= 6) ? 2 : 1;
     p.off_epi = stages * p.stage_stride;
     p.off_bar = p.off_epi + epi_bytes;
     p.smem_bytes = p.off_bar + kBarrierBytes + 1024;
@@ -281,6 +296,7 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->BN = p.BN; kp->stages = p.stages;
     kp->kgroup = p.kgroup;
     kp->bk = p.bk;
+    kp->m_sub = p.wide ? 2 : 1;
     kp->idesc = p.idesc;
     kp->a_mn_major = p.a.mn_major; kp->b_mn_major = p.b.mn_major;
     kp->a_nbox = p.a.nbox; kp->b_nbox = p.b.nbox;
@@ -317,7 +333,7 @@ std::string describe_json(const Plan& p) {
     };
     o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
       << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
-      << ",\"pair\":" << p.pair << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
+      << ",\"pair\":" << p.pair << ",\"wide\":" << p.wide << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
       << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads

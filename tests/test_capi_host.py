@@ -156,6 +156,37 @@ def test_planner_fp8_layouts_match_oracle(lib, am, bm, ind):
             assert op["box"] == ([128, tile] if not mn_major else [128, 128])
 
 
+@pytest.mark.parametrize("am", [0, 1])
+@pytest.mark.parametrize("bm", [0, 1])
+@pytest.mark.parametrize("ind", ["bf16", "e4m3"])
+def test_wide_pair_plans(lib, monkeypatch, am, bm, ind):
+    """Wide CTA pair (512 x 256 tiles): each CTA stages 256 rows of A, whose
+    second 128-row half starts 16 KiB into the stage in every layout (the
+    offset the issue loop adds); 4 stages of 48 KiB, one per barrier pair."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    es = 1 if ind == "e4m3" else 2
+    bk = 128 // es
+    for (M, N, K) in [(8192, 8192, 8192), (1500, 1152, 896), (129, 257, 65)]:
+        d = smo.gemm_plan_describe(M, N, K, am, bm, ind, "bf16")
+        assert d["ok"], d["why"]
+        assert d["pair"] and d["wide"] and d["BM"] == 512 and d["BN"] == 256
+        assert d["stages"] == 4 and d["kgroup"] == 1 and d["tmem_cols"] == 512
+        assert d["smem_bytes"] <= 232448
+        assert ((d["idesc"] >> 24) & 31) * 16 == 256 and ((d["idesc"] >> 17) & 63) * 8 == 256
+        A = d["A"]
+        assert A["tile_mn"] == 256 and A["stage_bytes"] == 256 * 128
+        assert A["linear"] and A["bijective"] and A["tma_equals_umma"] and A["core_matrix_divides"]
+        for mn in range(0, 256, 7):
+            for k in range(0, bk, 3):
+                off = banksim.operand_tile_offset(mn, k, bool(am), 256, elem_bytes=es, box_k=bk)
+                assert banksim.umma_canonical_offset(mn, k, bool(am), A["lbo"], A["sbo"], A["kstep_bytes"],
+                                                     elem_bytes=es, mma_k=32 // es) == off
+                if mn >= 128:       # the second half, read by descriptors 16 KiB further on
+                    assert off - banksim.operand_tile_offset(mn - 128, k, bool(am), 256, elem_bytes=es,
+                                                             box_k=bk) == 16384
+        assert d["B"]["tile_mn"] == 128 and d["stage_stride"] == 256 * 128 + 128 * 128
+
+
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_epilogue_stores_conflict_free(lib, out):
     d = smo.gemm_plan_describe(1024, 1024, 1024, 0, 1, "bf16", out)
@@ -212,16 +243,21 @@ def test_instruction_descriptor_fp8_fields(lib):
 def test_tile_choice_and_grid(lib):
     d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
     assert not d["pair"] and d["BN"] == 128 and d["tiles"] == 12 * 9 and d["grid"] == 108
+    # long K: the wide pair (512 x 256 tiles); short K: 256 x 256
     d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
-    assert d["pair"] and d["BM"] == 256 and d["BN"] == 256 and d["tiles"] == 32 * 32
+    assert d["pair"] and d["wide"] and d["BM"] == 512 and d["BN"] == 256 and d["tiles"] == 16 * 32
+    assert d["grid"] == 152 and d["stages"] == 4 and d["A"]["tile_mn"] == 256 and d["B"]["tile_mn"] == 128
+    d = smo.gemm_plan_describe(16384, 8192, 1024, 0, 1, "bf16", "bf16")
+    assert d["pair"] and not d["wide"] and d["BM"] == 256 and d["tiles"] == 64 * 32
     assert d["grid"] == 152 and d["stages"] == 6 and d["A"]["tile_mn"] == d["B"]["tile_mn"] == 128
     d = smo.gemm_plan_describe(2048, 2048, 2048, 0, 1, "bf16", "bf16", batch=32)
     assert d["pair"] and d["tiles"] == 8 * 8 * 32
 
 
-def test_pair_descriptors(lib):
+def test_pair_descriptors(lib, monkeypatch):
     """CTA pair: M = 256 and N = 256 in the instruction descriptor, each CTA
     stages 128 rows of A and 128 columns of B per 64-deep stage."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "512")
     for am in (0, 1):
         for bm in (0, 1):
             d = smo.gemm_plan_describe(8192, 8192, 8192, am, bm, "bf16", "bf16")

@@ -45,7 +45,7 @@ def test_small_ragged_all_orientations(am, bm, dt, out):
         _full(p)
 
 
-@pytest.mark.parametrize("mode", [128, 256, 512])
+@pytest.mark.parametrize("mode", [128, 256, 512, 1024])
 @pytest.mark.parametrize("am,bm", MAJORS)
 def test_tile_modes_ragged(monkeypatch, mode, am, bm):
     monkeypatch.setenv("SMO_GEMM_FORCE_BN", str(mode))

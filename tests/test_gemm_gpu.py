@@ -40,7 +40,7 @@ def force_mode(monkeypatch):
 
 
 # ------------------------------------------------------------ every tile mode
-@pytest.mark.parametrize("mode", [128, 256, 512])
+@pytest.mark.parametrize("mode", [128, 256, 512, 1024])
 @pytest.mark.parametrize("am,bm", MAJORS)
 def test_tile_modes_ragged(force_mode, mode, am, bm):
     force_mode(mode)
@@ -54,7 +54,7 @@ def test_tile_modes_ragged(force_mode, mode, am, bm):
         _full(p)
 
 
-@pytest.mark.parametrize("mode", [128, 256, 512])
+@pytest.mark.parametrize("mode", [128, 256, 512, 1024])
 def test_tile_modes_integer_and_permutation_exact(force_mode, mode):
     force_mode(mode)
     for am, bm in MAJORS:
@@ -70,7 +70,7 @@ def test_tile_modes_integer_and_permutation_exact(force_mode, mode):
         _full(q, exact=True)
 
 
-@pytest.mark.parametrize("mode", [128, 256, 512])
+@pytest.mark.parametrize("mode", [128, 256, 512, 1024])
 def test_tile_modes_batched_and_timeout(force_mode, mode):
     force_mode(mode)
     p = make_problem(300, 260, 200, batch=3, dist="normal", sigma=0.5, seed=4, out_dtype="bf16")
@@ -251,6 +251,21 @@ def _pair_tiles(M, N):
 def test_stream_k_tiles_full_compare(M, N, K, dist, monkeypatch):
     monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
     p = make_problem(M, N, K, a_major=K_MAJOR, b_major=MN_MAJOR, dist=dist, seed=M + K,
+                     out_dtype="f32" if dist == "int" else "bf16")
+    _full(p, exact=(dist == "int"))
+
+
+@pytest.mark.parametrize("M,N,K,dist", [
+    (5120, 4096, 512, "uniform"),     # 160 wide tiles: two whole waves + 8 tiles split
+    (2560, 2048, 520, "int"),         # 40 tiles, all split; K tail in the split range: bit-exact
+    (1800, 1100, 700, "normal"),      # ragged M, N
+])
+def test_stream_k_wide_tiles_full_compare(M, N, K, dist, monkeypatch):
+    """Stream-K on 512 x 256 tiles: each piece carries two accumulator regions
+    per CTA and every warp announces its partial once."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
+    p = make_problem(M, N, K, a_major=K_MAJOR, b_major=MN_MAJOR, dist=dist, seed=M + K + 1,
                      out_dtype="f32" if dist == "int" else "bf16")
     _full(p, exact=(dist == "int"))
 
