@@ -224,6 +224,78 @@ __device__ __forceinline__ void epilogue_partial(const KParams& p, uint32_t tmem
     if (lane == 0) atomicAdd(flag, 1);
 }
 
+// One 128-byte column chunk of the epilogue, step 1: read the warp's 32 rows
+// of it from tensor memory (fp32 output: 32 columns; 16-bit output: 64
+// columns, packed in pairs), adding any stream-K partials.
+template <int OUT>
+__device__ __forceinline__ void epi_load_chunk(uint32_t tmem_acc, uint32_t lane_field, int c, int lane,
+                                               const float* parts, int64_t part_stride, uint32_t part_mask,
+                                               uint32_t (&v)[32]) {
+    constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
+    const uint32_t col = (uint32_t)(c * kChunkCols);
+    if (OUT == OUT_F32) {
+        tmem_ld_32x32b_x32(tmem_acc + lane_field + col, v);
+        tmem_ld_wait();
+        if (parts) add_partials(v, parts, part_stride, part_mask, c, lane);
+    } else {
+        uint32_t r0[32], r1[32];
+        tmem_ld_32x32b_x32(tmem_acc + lane_field + col, r0);
+        tmem_ld_32x32b_x32(tmem_acc + lane_field + col + 32, r1);
+        tmem_ld_wait();
+        if (parts) {
+            add_partials(r0, parts, part_stride, part_mask, 2 * c, lane);
+            add_partials(r1, parts, part_stride, part_mask, 2 * c + 1, lane);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            v[i] = pack2<OUT>(r0[2 * i], r0[2 * i + 1]);
+            v[16 + i] = pack2<OUT>(r1[2 * i], r1[2 * i + 1]);
+        }
+    }
+}
+
+// Step 2: stage the chunk in this warp's swizzled slab and store it with TMA
+// (the ragged < 16-byte end of a row is copied from the slab directly).  The
+// caller has made sure the slab's previous store has finished reading it.
+template <int OUT>
+__device__ __forceinline__ void epi_store_chunk(const KParams& p, const CUtensorMap* tmC, uint32_t slab, int lane,
+                                                int32_t m0, int32_t nc, int b, const uint32_t (&v)[32]) {
+    constexpr int kOutBytes = (OUT == OUT_F32) ? 4 : 2;
+    constexpr int kChunkCols = 128 / kOutBytes;
+    // Row `lane` of the slab; 16-byte chunk j goes to j ^ (row % 8): the 8
+    // lanes of each store phase hit 8 different bank groups.
+    const uint32_t row = slab + (uint32_t)lane * 128u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        st_shared_v4(row + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (m0 < p.M && nc < p.n_tma) tma_store_3d(tmC, slab, nc, m0, b);
+        bulk_commit();
+    }
+    if (nc + kChunkCols > p.n_tma && nc < p.N) {
+        // TMA stores write whole 16-byte pieces at the row end; the last
+        // < 16 bytes of a ragged row are copied from this lane's own row of
+        // the swizzled slab (its own st.shared above are visible to it).
+        const int32_t m = m0 + lane;
+        if (m < p.M) {
+            char* rowp = static_cast<char*>(p.C) + ((int64_t)b * p.strideC + (int64_t)m * p.ldc) * kOutBytes;
+            const int32_t n_lo = max(p.n_tma, nc), n_hi = min(p.N, nc + kChunkCols);
+#pragma unroll 1
+            for (int32_t n = n_lo; n < n_hi; ++n) {
+                const uint32_t byte = (uint32_t)(n - nc) * kOutBytes;
+                const uint32_t src = row + ((((byte >> 4) ^ (uint32_t)(lane & 7)) << 4) | (byte & 15u));
+                if (OUT == OUT_F32)
+                    *reinterpret_cast<uint32_t*>(rowp + (int64_t)n * 4) = ld_shared_u32(src);
+                else
+                    *reinterpret_cast<uint16_t*>(rowp + (int64_t)n * 2) = ld_shared_u16(src);
+            }
+        }
+    }
+}
+
 // Epilogue of one accumulator tile for one warp: its 32 rows (TMEM lanes
 // 32*(warp % 4) ...), all p.epi_chunks column chunks of 128 bytes.
 //   tmem_acc : tensor-memory address of the accumulator (lane field 0)
@@ -237,72 +309,50 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
                                               int32_t m0, int32_t n0, int b, Release release,
                                               const float* parts = nullptr, int64_t part_stride = 0,
                                               uint32_t part_mask = 0) {
-    constexpr int kOutBytes = (OUT == OUT_F32) ? 4 : 2;
-    constexpr int kChunkCols = 128 / kOutBytes;
+    constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
     for (int c = 0; c < p.epi_chunks; ++c) {
         const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
         if (lane == 0) bulk_wait_read<1>();        // this slab's previous store has read it
         __syncwarp();
-        const uint32_t col = (uint32_t)(c * kChunkCols);
         uint32_t v[32];
-        if (OUT == OUT_F32) {
-            tmem_ld_32x32b_x32(tmem_acc + lane_field + col, v);
-            tmem_ld_wait();
-            if (parts) add_partials(v, parts, part_stride, part_mask, c, lane);
-        } else {
-            uint32_t r0[32], r1[32];
-            tmem_ld_32x32b_x32(tmem_acc + lane_field + col, r0);
-            tmem_ld_32x32b_x32(tmem_acc + lane_field + col + 32, r1);
-            tmem_ld_wait();
-            if (parts) {
-                add_partials(r0, parts, part_stride, part_mask, 2 * c, lane);
-                add_partials(r1, parts, part_stride, part_mask, 2 * c + 1, lane);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                v[i] = pack2<OUT>(r0[2 * i], r0[2 * i + 1]);
-                v[16 + i] = pack2<OUT>(r1[2 * i], r1[2 * i + 1]);
-            }
-        }
+        epi_load_chunk<OUT>(tmem_acc, lane_field, c, lane, parts, part_stride, part_mask, v);
         if (c == p.epi_chunks - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release();
         }
-        // Row `lane` of the slab; 16-byte chunk j goes to j ^ (row % 8): the 8
-        // lanes of each store phase hit 8 different bank groups.
-        const uint32_t row = slab + (uint32_t)lane * 128u;
+        epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
+        sbuf ^= 1u;
+    }
+}
+
+// The last accumulator region of a tile with 16-bit output and 256 columns
+// (4 chunks): all four chunks are read from tensor memory into registers
+// first (128 per thread, packed), the accumulator is released, and only then
+// are the chunks staged and stored -- the MMA issuer waits for four tensor
+// memory reads instead of four whole chunk round trips.
+template <int OUT, typename Release>
+__device__ __forceinline__ void epilogue_region_early_release(const KParams& p, const CUtensorMap* tmC,
+                                                              uint32_t tmem_acc, uint32_t lane_field,
+                                                              uint32_t slabs, uint32_t& sbuf, int lane, int32_t m0,
+                                                              int32_t n0, int b, Release release,
+                                                              const float* parts, int64_t part_stride,
+                                                              uint32_t part_mask) {
+    static_assert(OUT != OUT_F32, "16-bit output: 64 columns per chunk");
+    constexpr int kChunks = 4;                      // 256 columns
+    uint32_t v[kChunks][32];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            st_shared_v4(row + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                         v[4 * j + 3]);
-        }
-        fence_proxy_async_smem();
+    for (int c = 0; c < kChunks; ++c)
+        epi_load_chunk<OUT>(tmem_acc, lane_field, c, lane, parts, part_stride, part_mask, v[c]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release();
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+        const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
+        if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
-        const int32_t nc = n0 + c * kChunkCols;
-        if (lane == 0) {
-            if (m0 < p.M && nc < p.n_tma) tma_store_3d(tmC, slab, nc, m0, b);
-            bulk_commit();
-        }
-        if (nc + kChunkCols > p.n_tma && nc < p.N) {
-            // TMA stores write whole 16-byte pieces at the row end; the last
-            // < 16 bytes of a ragged row are copied from this lane's own row of
-            // the swizzled slab (its own st.shared above are visible to it).
-            const int32_t m = m0 + lane;
-            if (m < p.M) {
-                char* rowp = static_cast<char*>(p.C) + ((int64_t)b * p.strideC + (int64_t)m * p.ldc) * kOutBytes;
-                const int32_t n_lo = max(p.n_tma, nc), n_hi = min(p.N, nc + kChunkCols);
-#pragma unroll 1
-                for (int32_t n = n_lo; n < n_hi; ++n) {
-                    const uint32_t byte = (uint32_t)(n - nc) * kOutBytes;
-                    const uint32_t src = row + ((((byte >> 4) ^ (uint32_t)(lane & 7)) << 4) | (byte & 15u));
-                    if (OUT == OUT_F32)
-                        *reinterpret_cast<uint32_t*>(rowp + (int64_t)n * 4) = ld_shared_u32(src);
-                    else
-                        *reinterpret_cast<uint16_t*>(rowp + (int64_t)n * 2) = ld_shared_u16(src);
-                }
-            }
-        }
+        epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * 64, b, v[c]);
         sbuf ^= 1u;
     }
 }

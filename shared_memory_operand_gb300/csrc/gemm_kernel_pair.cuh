@@ -327,12 +327,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // CTA `rank`'s accumulator region i holds tile rows rank * 128 * MSUB + i * 128 ...
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
                                    (int32_t)q * kEpiRowsPerWarp;
+                const float* parts = mask ? p.sk_work + (cluster_id + 1) * slot_floats + warp_rows(i) : nullptr;
+                if constexpr (WIDE && OUT != OUT_F32) {
+                    if (i == MSUB - 1) {
+                        // the single accumulator: hand it back to the MMA issuer
+                        // as soon as the last region sits in registers
+                        epilogue_region_early_release<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
+                                                           sbuf, lane, m0, nb * p.BN, b,
+                                                           [&] { mbar_arrive_cluster(acce); }, parts, slot_floats,
+                                                           mask);
+                        continue;
+                    }
+                }
                 epilogue_tile<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs, sbuf, lane, m0, nb * p.BN,
                                    b, [&] {
                                        if (i == MSUB - 1) mbar_arrive_cluster(acce);
                                    },
-                                   mask ? p.sk_work + (cluster_id + 1) * slot_floats + warp_rows(i) : nullptr,
-                                   slot_floats, mask);
+                                   parts, slot_floats, mask);
             }
         }
         if (lane == 0) bulk_wait<0>();
