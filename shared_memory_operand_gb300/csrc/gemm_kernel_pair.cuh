@@ -1,20 +1,22 @@
-// CTA-pair variant of the persistent GEMM for sm_103a: 256 x 256 output tiles
-// computed by two CTAs of a cluster with tcgen05.mma.cta_group::2.
+// CTA-pair variant of the persistent GEMM for sm_103a: output tiles computed
+// by two CTAs of a cluster with tcgen05.mma.cta_group::2 (256 x 256 x K_mma
+// per instruction).
 //
-// Each CTA of the pair holds its own 128 rows of A and its own 128 columns of
-// B per pipeline stage (32 KiB per stage, 6 stages); the even CTA's single MMA
-// thread issues 256 x 256 x 16 MMAs that read both CTAs' shared memory and
-// accumulate rows 0..127 in the even CTA's tensor memory and rows 128..255 in
-// the odd CTA's.  Compared with one CTA per 128 x 256 tile this halves the
-// B bytes each SM stages per flop and doubles the pipeline depth for the same
-// shared memory ("An Educational GEMM Ladder for Helios GPUs", Level 4: larger
-// output tiles raise arithmetic intensity; Level 9: a cluster of workgroups
-// shares operand panels instead of re-requesting them).
-//
-// The ring's stages are handed over in groups of two: one full/empty barrier
-// pair, one wait and one commit per group of 2 x 4 MMAs.  A single thread issues every MMA, and with a wait and
-// a commit per 4 MMAs its instruction latency, not the tensor pipe, set the
-// pace.
+// Each CTA of the pair holds its own rows of A and its own 128 columns of B
+// per pipeline stage; the even CTA's single MMA thread issues MMAs that read
+// both CTAs' shared memory and accumulate the even CTA's rows in its tensor
+// memory and the odd CTA's rows in the odd CTA's.  Compared with one CTA per
+// 128 x 256 tile this halves the B bytes each SM stages per flop and doubles
+// the pipeline depth for the same shared memory ("An Educational GEMM Ladder
+// for Helios GPUs", Level 4: larger output tiles raise arithmetic intensity;
+// Level 9: a cluster of workgroups shares operand panels instead of
+// re-requesting them).  Two tile shapes (template parameter WIDE):
+//   256 x 256: 128 A rows per CTA, 6 stages of 32 KiB handed over two at a
+//              time (one full/empty barrier pair, one wait and one commit per
+//              8 MMAs: the single issuing thread, not the tensor pipe, set the
+//              pace with a wait and a commit per 4), two accumulators;
+//   512 x 256: 256 A rows per CTA in two 128-row halves with their own MMAs,
+//              4 stages of 48 KiB, one accumulator of 512 columns.
 //
 // Synchronisation across the pair:
 //   full[g]    (even CTA only) -- both CTAs' TMA loads of the group complete
