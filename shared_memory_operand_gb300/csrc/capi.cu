@@ -223,8 +223,23 @@ int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const 
         }
         ds.attr_set[slot] = true;
     }
-    kern<<<pl.grid, smo::kThreads, pl.smem_bytes, stream>>>(ta, tb, tc, kp);
-    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+    // programmatic stream serialization: the kernel's prologue may overlap the
+    // previous kernel's tail (the kernel waits for it before touching memory)
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3(smo::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
     return GEMM_OK;
 }
 
@@ -246,16 +261,19 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     const int slot = (WIDE * 2 + KIND) * 3 + OUT;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the prologue may overlap the previous kernel (see launch_single_kg)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(smo::kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (!ds.pair_attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
             cudaSuccess) {

@@ -95,6 +95,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     cluster_sync_all();
     tc_fence_after();
+    // The prologue above touches only shared memory, tensor memory and the
+    // kernel parameters, so it may overlap the previous kernel in the stream
+    // (launched with programmatic stream serialization); every global memory
+    // access comes after this wait.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = ld_shared_u32(tmem_slot);
     const int64_t budget = p.timeout_ns;
     const int64_t cluster_id = blockIdx.x >> 1;

@@ -270,4 +270,15 @@ __device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t cta_m
         : "memory");
 }
 
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// griddep_wait: block until every grid this one depends on (the previous
+// kernel in the stream) has completed and its memory operations are visible.
+// griddep_launch_dependents: allow the next kernel in the stream to be
+// scheduled now; it runs its own prologue on SMs this grid has left and then
+// waits in griddep_wait.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 }  // namespace smo

@@ -163,6 +163,30 @@ def test_side_stream_and_repeat():
             check(p, run_gpu(p, stream=s), ref)
 
 
+@pytest.mark.parametrize("n,steps", [(512, 20), (4096, 6)])
+def test_dependent_chain_without_host_sync(n, steps):
+    """C_{i+1} = C_i * P on one stream with no synchronisation in between:
+    each launch's prologue may overlap the previous kernel (programmatic
+    stream serialization) but must read its output only after it completed.
+    P is a permutation and the entries small integers, so every step is exact
+    (4096: the wide-tile kernel)."""
+    g = torch.Generator().manual_seed(n)
+    A0 = torch.randint(-1, 2, (n, n), generator=g).float()
+    P = torch.zeros(n, n)
+    P[torch.arange(n), torch.randperm(n, generator=g)] = 1.0
+    cur = A0.to(torch.bfloat16).cuda()
+    Pd = P.to(torch.bfloat16).cuda()
+    for _ in range(steps):
+        nxt = torch.empty(n, n, dtype=torch.bfloat16, device="cuda")
+        smo.gemm_ex(cur, n, K_MAJOR, Pd, n, MN_MAJOR, nxt, n, n, n, n, in_dtype="bf16", out_dtype="bf16")
+        cur = nxt
+    assert smo.gemm_check(None) == smo.GEMM_OK
+    want = A0.double()
+    for _ in range(steps):
+        want = want @ P.double()
+    assert torch.equal(cur.double().cpu(), want)
+
+
 def test_gemm_bf16_entry_point():
     p = make_problem(256, 256, 256, dist="uniform", out_dtype="f32")
 
