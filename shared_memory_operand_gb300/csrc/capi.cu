@@ -147,16 +147,19 @@ int validate(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_d
     return GEMM_OK;
 }
 
-const Plan* cached_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype, int out_dtype,
-                        int64_t batch, int num_sms) {
+// The plan for these arguments, from the cache (a copy: the cache may be
+// cleared by another thread while this one launches).
+Plan cached_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype, int out_dtype,
+                 int64_t batch, int num_sms) {
     int fbn = force_bn_from_env();
     PlanKey key{M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn};
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
-    if (it != g_plans.end()) return &it->second;
+    if (it != g_plans.end()) return it->second;
     if (g_plans.size() > 4096) g_plans.clear();
     Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn);
-    return &(g_plans[key] = p);
+    g_plans[key] = p;
+    return p;
 }
 
 uint64_t batch_stride_bytes(uint64_t es, uint64_t ld, uint64_t outer, uint64_t batch, uint64_t stride) {
@@ -215,13 +218,16 @@ int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const 
                      const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
     auto kern = smo::smo_gemm_kernel<OUT, KG, KIND>;
     const int slot = (KIND * 3 + OUT) * 2 + KG - 1;
-    if (!ds.attr_set[slot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);     // once per device and kernel variant
+        if (!ds.attr_set[slot]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+            ds.attr_set[slot] = true;
         }
-        ds.attr_set[slot] = true;
     }
     // programmatic stream serialization: the kernel's prologue may overlap the
     // previous kernel's tail (the kernel waits for it before touching memory)
@@ -274,22 +280,26 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    if (!ds.pair_attr_set[slot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
+    int64_t maxc = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);     // once per device and kernel variant
+        if (!ds.pair_attr_set[slot]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+            cfg.gridDim = dim3(2 * (unsigned)std::max(1, ds.num_sms / 2), 1, 1);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+                cudaGetLastError();
+                return GEMM_ERR_LAUNCH;
+            }
+            ds.pair_max_clusters[slot] = n;
+            ds.pair_attr_set[slot] = true;
         }
-        cfg.gridDim = dim3(2 * (unsigned)std::max(1, ds.num_sms / 2), 1, 1);
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-        ds.pair_max_clusters[slot] = n;
-        ds.pair_attr_set[slot] = true;
+        maxc = ds.pair_max_clusters[slot];
     }
-    const int64_t maxc = ds.pair_max_clusters[slot];
     int64_t clusters = std::min<int64_t>(pl.tiles, maxc);
     kp.sk_clusters = 0;
     kp.dp_tiles = pl.tiles;
@@ -306,11 +316,11 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
         // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
         if (worth && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
             const size_t work_bytes = (size_t)maxc * (size_t)pl.tile_m * (size_t)pl.BN * sizeof(float);
-            DevState::SkWork* w = nullptr;
-            {
-                std::lock_guard<std::mutex> lk(g_mu);
-                w = &ds.sk[stream];
-            }
+            // The stream's workspace is looked up and grown under the lock, so
+            // that host threads launching on the same stream never free a
+            // buffer another one has just handed to a kernel.
+            std::lock_guard<std::mutex> lk(g_mu);
+            DevState::SkWork* w = &ds.sk[stream];
             // No allocation inside a stream capture: a capturing stream without
             // a large enough workspace yet runs this GEMM without stream-K.
             cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -476,7 +486,8 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
         }
         return GEMM_OK;
     }
-    const Plan* pl = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, ds.num_sms);
+    const Plan plan = cached_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, ds.num_sms);
+    const Plan* pl = &plan;
     if (!pl->ok) return GEMM_ERR_UNSUPPORTED;
 
     // TMA stores write whole 16-byte pieces, so the C map covers only the

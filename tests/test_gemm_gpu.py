@@ -187,6 +187,42 @@ def test_dependent_chain_without_host_sync(n, steps):
     assert torch.equal(cur.double().cpu(), want)
 
 
+def test_concurrent_host_threads(monkeypatch):
+    """Host threads launching at once (the binding releases the interpreter
+    lock in the C calls): plan cache, per-variant launch state and the
+    stream-K workspace are shared; every result must still be exact."""
+    import threading
+    monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    shapes = [(2560, 2048, 520), (1024, 1024, 640), (300, 700, 900), (4096, 512, 256)]
+    errors = []
+
+    def worker(t):
+        try:
+            for j in range(6):
+                M, N, K = shapes[(t + j) % len(shapes)]
+                p = make_problem(M, N, K, dist="int", out_dtype="f32", seed=100 * t + j)
+                s = streams[t % len(streams)]              # threads 0 and 3 share a stream
+                with torch.cuda.stream(s):
+                    A, B = p.A.cuda(), p.B.cuda()
+                    C = torch.empty(p.c_numel(), dtype=torch.float32, device="cuda")
+                    smo.gemm_ex(A, p.lda, p.a_major, B, p.ldb, p.b_major, C, p.ldc, M, N, K,
+                                in_dtype="bf16", out_dtype="f32", stream=s)
+                    s.synchronize()
+                gpu = C.cpu().view(M, p.ldc)[:, :N].double().numpy()[None]
+                check(p, gpu, oracle_full(p), exact=True)
+        except Exception as e:          # noqa: BLE001 -- reported on the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert smo.gemm_check(None) == smo.GEMM_OK
+
+
 def test_gemm_bf16_entry_point():
     p = make_problem(256, 256, 256, dist="uniform", out_dtype="f32")
 
