@@ -437,7 +437,8 @@ def run_ours(args, world, rank, local):
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": peak_note,
                 "frac_of_sustained": achieved / peak_sus, "algorithmic_bytes": alg_bytes,
-                "kernel": KERNEL_NAME, "launch_ms_median": statistics.median(launch_ms)}
+                "kernel": KERNEL_NAME, "launch_ms_median": statistics.median(launch_ms),
+                "launch_ms_best": min(launch_ms)}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -483,7 +484,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
