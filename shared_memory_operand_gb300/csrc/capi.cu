@@ -314,7 +314,11 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
         // Wide tiles (512 KiB partials) lost 3.5% at 8192^3: automatic only on 256 x 256 tiles.
         const bool worth = stream_k == 1 || (!pl.wide && (sk_tiles * (int64_t)pl.num_k) / maxc >= 48);
         // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
-        if (worth && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
+        // The owner streams the partials through the idle operand ring
+        // (kFixRingBytes) in blocks of 128 accumulator columns.
+        const bool fits = (size_t)pl.stages * pl.stage_stride >= smo::kFixRingBytes &&
+                          pl.BN % (32 * smo::kFixChunks) == 0;
+        if (worth && fits && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
             const size_t work_bytes = (size_t)maxc * (size_t)pl.tile_m * (size_t)pl.BN * sizeof(float);
             // The stream's workspace is looked up and grown under the lock, so
             // that host threads launching on the same stream never free a

@@ -177,35 +177,27 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) {
     }
 }
 
-// Partial accumulators are stored in the order a warp holds them after
-// tcgen05.ld.32x32b: for 32-column chunk j, column i of lane l (the warp's
-// row l) at [(j * 32 + i) * 32 + l] -- every store and load of a warp is one
-// contiguous 128-byte line.
+// Stream-K partials.  A warp's partial of one accumulator region (its 32
+// rows, BN fp32 columns) is BN / 32 blocks of 4 KiB, one per 32-column chunk,
+// each laid out like an fp32 epilogue slab: row r (the warp's lane r) is 128
+// bytes and its 16-byte piece j sits at piece j ^ (r % 8).  Written from and
+// read into shared memory with 16-byte accesses, every 8 lanes of an access
+// phase hit 8 different bank groups; between shared and global memory the
+// blocks move as plain bulk copies.
 
-// acc[i] (fp32 bits) += slot_s[(chunk32 * 32 + i) * 32 + lane] for every slot
-// s set in `mask`, in increasing slot order (a fixed order: the sum does not
-// depend on timing).
-__device__ __forceinline__ void add_partials(uint32_t (&acc)[32], const float* parts, int64_t stride,
-                                             uint32_t mask, int chunk32, int lane) {
-    for (uint32_t m = mask; m; m &= m - 1) {
-        const int s = __ffs(m) - 1;
-        const float* src = parts + (int64_t)s * stride + (int64_t)chunk32 * 32 * 32 + lane;
-        float q[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) q[i] = __ldcg(src + i * 32);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = __float_as_uint(__uint_as_float(acc[i]) + q[i]);
-    }
-}
-
-// Stream-K partial piece: this warp's 32 accumulator rows (all BN columns,
-// fp32) go to `dst` in the order above; with `announce` the warp then
-// publishes everything it has written on `flag`.  `release` is called once
-// the accumulator region has been read.
+// Writes the warp's partial of one region (tensor memory `tmem_acc`) to `dst`
+// through its staging slabs; `release` is called once the region has been
+// read.  With `announce` the warp then waits for its copies to land and adds
+// 1 to `flag`.
 template <typename Release>
 __device__ __forceinline__ void epilogue_partial(const KParams& p, uint32_t tmem_acc, uint32_t lane_field, int lane,
-                                                 float* dst, int32_t* flag, bool announce, Release release) {
+                                                 uint32_t slabs, uint32_t& sbuf, float* dst, int32_t* flag,
+                                                 bool announce, Release release) {
+    const uint32_t row = (uint32_t)lane * 128u;
     for (int c = 0; c < p.BN / 32; ++c) {
+        const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
+        if (lane == 0) bulk_wait_read<1>();        // this slab's previous copy has read it
+        __syncwarp();
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_acc + lane_field + (uint32_t)(c * 32), v);
         tmem_ld_wait();
@@ -214,38 +206,124 @@ __device__ __forceinline__ void epilogue_partial(const KParams& p, uint32_t tmem
             __syncwarp();
             if (lane == 0) release();
         }
-        float* out = dst + (int64_t)c * 32 * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) __stcg(out + i * 32, __uint_as_float(v[i]));
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(slab + row + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_store(dst + (int64_t)c * 32 * 32, slab, kEpiSlabBytes);
+            bulk_commit();
+        }
+        sbuf ^= 1u;
     }
     if (!announce) return;
-    __threadfence();
+    if (lane == 0) {
+        bulk_wait<0>();             // every copy of this warp has landed
+        fence_proxy_async_all();    // ... and comes before the generic release below
+        __threadfence();
+        atomicAdd(flag, 1);
+    }
     __syncwarp();
-    if (lane == 0) atomicAdd(flag, 1);
+}
+
+// Stream-K fix-up of one epilogue warp: adds the partials of the slots set in
+// `mask` to its 32 accumulator rows of regions 0 .. nreg-1 (256 tensor memory
+// columns apart), slot by slot in increasing order -- a fixed order, so the
+// sum does not depend on timing.  The partials arrive in blocks of kFixChunks
+// chunks, copied by bulk loads into the warp's kFixBufs buffers kFixBufs
+// blocks ahead of the additions; every warp streams only its own rows.
+//   parts        : the warp's partial of region 0 in slot 0
+//   slot_stride  : floats from one slot to the next; region_stride likewise
+//   bufs, bars   : the warp's first buffer and first mbarrier (count 1)
+// The buffers lie in the operand ring: the owner's piece is the last piece of
+// its cluster's range, so once its accumulator is full no load or MMA touches
+// the ring again.  Returns false if a copy did not land within the budget
+// (the copies still in flight are then waited for, again with the budget).
+__device__ __forceinline__ bool sk_fixup(uint32_t tmem_acc, uint32_t lane_field, int lane, int BN, int nreg,
+                                        const float* parts, int64_t slot_stride, int64_t region_stride,
+                                        uint32_t mask, uint32_t bufs, uint32_t bars, int64_t budget) {
+    const int nh = BN / (32 * kFixChunks);          // blocks per region and slot
+    const int ns = __popc(mask);
+    const int nb = nreg * ns * nh;
+    // block b: part h, k-th slot of the mask, region i (region-major order)
+    auto src_of = [&](int b) {
+        const int h = b % nh, t = b / nh, k = t % ns, i = t / ns;
+        uint32_t m = mask;
+        for (int j = 0; j < k; ++j) m &= m - 1;
+        return parts + (int64_t)(__ffs(m) - 1) * slot_stride + (int64_t)i * region_stride +
+               (int64_t)h * (kFixChunks * 32 * 32);
+    };
+    if (lane == 0) {
+        fence_proxy_async_all();    // the partials were acquired through the generic proxy
+        for (int b = 0; b < nb && b < kFixBufs; ++b) {
+            mbar_arrive_expect_tx(bars + 8u * b, kFixBlockBytes);
+            bulk_load(bufs + b * kFixBlockBytes, src_of(b), kFixBlockBytes, bars + 8u * b);
+        }
+    }
+    const uint32_t row = (uint32_t)lane * 128u;
+    for (int b = 0; b < nb; ++b) {
+        const int j = b % kFixBufs;
+        const uint32_t buf = bufs + j * kFixBlockBytes;
+        if (!__all_sync(0xffffffffu, mbar_wait(bars + 8u * j, (uint32_t)(b / kFixBufs) & 1u, budget))) {
+            if (lane == 0)
+                for (int r = b + 1; r < nb && r < b + kFixBufs; ++r)
+                    (void)mbar_wait(bars + 8u * (r % kFixBufs), (uint32_t)(r / kFixBufs) & 1u, budget);
+            return false;
+        }
+        const int h = b % nh, i = (b / nh) / ns;
+        const uint32_t col0 = (uint32_t)(i * 256 + h * kFixChunks * 32);
+#pragma unroll 1
+        for (int cc = 0; cc < kFixChunks; cc += 2) {
+            const uint32_t taddr = tmem_acc + lane_field + col0 + (uint32_t)(cc * 32);
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(taddr, v0);
+            tmem_ld_32x32b_x32(taddr + 32, v1);
+            tmem_ld_wait();
+            const uint32_t s0 = buf + (uint32_t)cc * kEpiSlabBytes + row, s1 = s0 + kEpiSlabBytes;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t piece = (uint32_t)(q ^ (lane & 7)) << 4;
+                const uint4 a = ld_shared_v4(s0 + piece), c = ld_shared_v4(s1 + piece);
+                v0[4 * q] = __float_as_uint(__uint_as_float(v0[4 * q]) + __uint_as_float(a.x));
+                v0[4 * q + 1] = __float_as_uint(__uint_as_float(v0[4 * q + 1]) + __uint_as_float(a.y));
+                v0[4 * q + 2] = __float_as_uint(__uint_as_float(v0[4 * q + 2]) + __uint_as_float(a.z));
+                v0[4 * q + 3] = __float_as_uint(__uint_as_float(v0[4 * q + 3]) + __uint_as_float(a.w));
+                v1[4 * q] = __float_as_uint(__uint_as_float(v1[4 * q]) + __uint_as_float(c.x));
+                v1[4 * q + 1] = __float_as_uint(__uint_as_float(v1[4 * q + 1]) + __uint_as_float(c.y));
+                v1[4 * q + 2] = __float_as_uint(__uint_as_float(v1[4 * q + 2]) + __uint_as_float(c.z));
+                v1[4 * q + 3] = __float_as_uint(__uint_as_float(v1[4 * q + 3]) + __uint_as_float(c.w));
+            }
+            tmem_st_32x32b_x32(taddr, v0);
+            tmem_st_32x32b_x32(taddr + 32, v1);
+        }
+        tmem_st_wait();
+        __syncwarp();
+        if (lane == 0 && b + kFixBufs < nb) {
+            fence_proxy_async_smem();   // the lanes' reads of this buffer come before the next copy
+            mbar_arrive_expect_tx(bars + 8u * j, kFixBlockBytes);
+            bulk_load(buf, src_of(b + kFixBufs), kFixBlockBytes, bars + 8u * j);
+        }
+    }
+    return true;
 }
 
 // One 128-byte column chunk of the epilogue, step 1: read the warp's 32 rows
 // of it from tensor memory (fp32 output: 32 columns; 16-bit output: 64
-// columns, packed in pairs), adding any stream-K partials.
+// columns, packed in pairs).
 template <int OUT>
-__device__ __forceinline__ void epi_load_chunk(uint32_t tmem_acc, uint32_t lane_field, int c, int lane,
-                                               const float* parts, int64_t part_stride, uint32_t part_mask,
-                                               uint32_t (&v)[32]) {
+__device__ __forceinline__ void epi_load_chunk(uint32_t tmem_acc, uint32_t lane_field, int c, uint32_t (&v)[32]) {
     constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
     const uint32_t col = (uint32_t)(c * kChunkCols);
     if (OUT == OUT_F32) {
         tmem_ld_32x32b_x32(tmem_acc + lane_field + col, v);
         tmem_ld_wait();
-        if (parts) add_partials(v, parts, part_stride, part_mask, c, lane);
     } else {
         uint32_t r0[32], r1[32];
         tmem_ld_32x32b_x32(tmem_acc + lane_field + col, r0);
         tmem_ld_32x32b_x32(tmem_acc + lane_field + col + 32, r1);
         tmem_ld_wait();
-        if (parts) {
-            add_partials(r0, parts, part_stride, part_mask, 2 * c, lane);
-            add_partials(r1, parts, part_stride, part_mask, 2 * c + 1, lane);
-        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             v[i] = pack2<OUT>(r0[2 * i], r0[2 * i + 1]);
@@ -306,16 +384,14 @@ __device__ __forceinline__ void epi_store_chunk(const KParams& p, const CUtensor
 template <int OUT, typename Release>
 __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
                                               uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
-                                              int32_t m0, int32_t n0, int b, Release release,
-                                              const float* parts = nullptr, int64_t part_stride = 0,
-                                              uint32_t part_mask = 0) {
+                                              int32_t m0, int32_t n0, int b, Release release) {
     constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
     for (int c = 0; c < p.epi_chunks; ++c) {
         const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
         if (lane == 0) bulk_wait_read<1>();        // this slab's previous store has read it
         __syncwarp();
         uint32_t v[32];
-        epi_load_chunk<OUT>(tmem_acc, lane_field, c, lane, parts, part_stride, part_mask, v);
+        epi_load_chunk<OUT>(tmem_acc, lane_field, c, v);
         if (c == p.epi_chunks - 1) {
             tc_fence_before();
             __syncwarp();
@@ -335,15 +411,13 @@ template <int OUT, typename Release>
 __device__ __forceinline__ void epilogue_region_early_release(const KParams& p, const CUtensorMap* tmC,
                                                               uint32_t tmem_acc, uint32_t lane_field,
                                                               uint32_t slabs, uint32_t& sbuf, int lane, int32_t m0,
-                                                              int32_t n0, int b, Release release,
-                                                              const float* parts, int64_t part_stride,
-                                                              uint32_t part_mask) {
+                                                              int32_t n0, int b, Release release) {
     static_assert(OUT != OUT_F32, "16-bit output: 64 columns per chunk");
     constexpr int kChunks = 4;                      // 256 columns
     uint32_t v[kChunks][32];
 #pragma unroll
     for (int c = 0; c < kChunks; ++c)
-        epi_load_chunk<OUT>(tmem_acc, lane_field, c, lane, parts, part_stride, part_mask, v[c]);
+        epi_load_chunk<OUT>(tmem_acc, lane_field, c, v[c]);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) release();

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * kMaxStages + 2 + b); };
     const uint32_t drain_bar = bars + 8u * (2 * kMaxStages + 4);
     const uint32_t tmem_slot = bars + 8u * (2 * kMaxStages + 5);
+    auto fix_bar = [&](uint32_t j) { return bars + 8u * (2 * kMaxStages + 6 + j); };   // kEpiWarps x kFixBufs
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acce_bar(b), 2 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        for (int j = 0; j < kEpiWarps * kFixBufs; ++j) mbar_init(fix_bar(j), 1);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -289,11 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t acce = mapa_shared(acce_bar(buf), lead);
             const uint32_t acc = tmem_base + buf * (uint32_t)p.BN;
+            const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
             if (w.role == ROLE_PARTIAL) {
                 // later K blocks of a stream-K tile: publish the fp32 partial
                 // (the warp announces it once, after its last region)
                 for (int i = 0; i < MSUB; ++i) {
-                    epilogue_partial(p, acc + (uint32_t)(i * 256), lane_field, lane,
+                    epilogue_partial(p, acc + (uint32_t)(i * 256), lane_field, lane, slabs, sbuf,
                                      p.sk_work + cluster_id * slot_floats + warp_rows(i), p.sk_flags + w.sk_tile,
                                      i == MSUB - 1, [&] {
                                          if (i == MSUB - 1) mbar_arrive_cluster(acce);
@@ -325,33 +328,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ready = __shfl_sync(0xffffffffu, ready, 0);
                 if (!ready) {
                     if (lane == 0) report_error(p.err, DEV_TIMEOUT_FIXUP);
-                    mask = 0;
-                } else {
-                    (void)ld_acquire_gpu(p.sk_flags + w.sk_tile);    // every lane acquires
+                } else if (mask != 0 &&
+                           !sk_fixup(acc, lane_field, lane, p.BN, MSUB,
+                                     p.sk_work + (cluster_id + 1) * slot_floats + warp_rows(0), slot_floats,
+                                     (int64_t)kEpiWarps * kEpiRowsPerWarp * p.BN, mask,
+                                     base + q * (kFixBufs * kFixBlockBytes), fix_bar(q * kFixBufs), budget)) {
+                    if (lane == 0) report_error(p.err, DEV_TIMEOUT_FIXUP);
                 }
             }
-            const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
             for (int i = 0; i < MSUB; ++i) {
                 // CTA `rank`'s accumulator region i holds tile rows rank * 128 * MSUB + i * 128 ...
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
                                    (int32_t)q * kEpiRowsPerWarp;
-                const float* parts = mask ? p.sk_work + (cluster_id + 1) * slot_floats + warp_rows(i) : nullptr;
                 if constexpr (WIDE && OUT != OUT_F32) {
                     if (i == MSUB - 1) {
                         // the single accumulator: hand it back to the MMA issuer
                         // as soon as the last region sits in registers
                         epilogue_region_early_release<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
                                                            sbuf, lane, m0, nb * p.BN, b,
-                                                           [&] { mbar_arrive_cluster(acce); }, parts, slot_floats,
-                                                           mask);
+                                                           [&] { mbar_arrive_cluster(acce); });
                         continue;
                     }
                 }
                 epilogue_tile<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs, sbuf, lane, m0, nb * p.BN,
                                    b, [&] {
                                        if (i == MSUB - 1) mbar_arrive_cluster(acce);
-                                   },
-                                   parts, slot_floats, mask);
+                                   });
             }
         }
         if (lane == 0) bulk_wait<0>();

@@ -16,7 +16,14 @@ constexpr int kEpiBufs = 2;         // staging buffers per epilogue warp
 constexpr uint32_t kEpiSlabBytes = kEpiRowsPerWarp * 128;   // 32 rows x 128 B
 constexpr int kMaxStages = 8;
 constexpr uint32_t kSmemLimit = 232448;                      // 227 KiB opt-in per block
-constexpr uint32_t kBarrierBytes = 256;
+constexpr uint32_t kBarrierBytes = 512;
+// Stream-K fix-up: each epilogue warp streams the fp32 partials it adds in
+// blocks of 4 accumulator column chunks (32 rows x 128 columns x 4 B) through
+// kFixBufs buffers of its own in the operand ring, idle by then.
+constexpr int kFixBufs = 3;
+constexpr int kFixChunks = 4;
+constexpr uint32_t kFixBlockBytes = kEpiRowsPerWarp * 32 * 4 * kFixChunks;    // 16 KiB
+constexpr uint32_t kFixRingBytes = kEpiWarps * kFixBufs * kFixBlockBytes;   // 192 KiB
 
 // Out element types.
 enum OutKind { OUT_F32 = 0, OUT_BF16 = 1, OUT_F16 = 2 };
