@@ -70,19 +70,42 @@ def kernel_source_hash(csrc: str = None) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if it was taken on the current kernel source (else None)."""
+def profiled_counters(workload: str) -> dict:
+    """The `name: number` lines of the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel source (else {})."""
     path = os.path.join(ROOT, "profiles", f"{KERNEL_NAME}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
-        return None
+        return {}
     src = re.search(r"^kernel_source_hash:\s*(\S+)", text, re.M)
-    val = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-    if not src or not val or src.group(1) != kernel_source_hash():
+    if not src or src.group(1) != kernel_source_hash():
+        return {}
+    return {m.group(1): float(m.group(2))
+            for m in re.finditer(r"^([a-z_]+):\s*([0-9][0-9.eE+]*)\s*$", text, re.M)}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary (None if absent or stale)."""
+    return profiled_counters(workload).get("dram_bytes_per_launch")
+
+
+def profiled_bank_conflicts(workload: str):
+    """Shared-memory bank conflicts per request of the GEMM kernel, from the
+    same ncu summary (None if absent or stale).  `excess_wavefronts` is ncu's
+    count of wavefronts above what the access pattern needs (actual minus
+    ideal), which excludes contention with the tensor core's and TMA's
+    shared-memory traffic; the l1tex conflict counters include it."""
+    c = profiled_counters(workload)
+    keys = ("smem_st_requests", "smem_st_bank_conflicts", "smem_ld_requests", "smem_ld_bank_conflicts",
+            "smem_excess_wavefronts")
+    if not all(k in c for k in keys):
         return None
-    return float(val.group(1))
+    return {"st_per_request": c["smem_st_bank_conflicts"] / max(c["smem_st_requests"], 1.0),
+            "ld_per_request": c["smem_ld_bank_conflicts"] / max(c["smem_ld_requests"], 1.0),
+            "st_requests": int(c["smem_st_requests"]), "ld_requests": int(c["smem_ld_requests"]),
+            "excess_wavefronts": int(c["smem_excess_wavefronts"]),
+            "source": f"ncu, profiles/{KERNEL_NAME}_{workload}.md"}
 
 
 class ClockSampler:
@@ -433,6 +456,7 @@ def run_ours(args, world, rank, local):
         peak_note += " x 2 (nominal dense FP8 / BF16 ratio 4.5 / 2.25)"
     alg_bytes = (p.M * p.K + p.K * p.N) * p.A.element_size() * p.batch + p.M * p.N * C.element_size() * p.batch
     traffic = profiled_traffic(args.workload)
+    conflicts = profiled_bank_conflicts(args.workload)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": peak_note,
@@ -467,6 +491,7 @@ def run_ours(args, world, rank, local):
                    ("pct_of_dense_fp8_peak" if fp8 else "pct_of_dense_bf16_peak"):
                        100.0 * agg["value"] / world / peak},
         "roofline": roofline,
+        "smem_bank_conflicts": conflicts,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps,
