@@ -113,6 +113,12 @@ def _store(logical: torch.Tensor, mn_major: bool, ld: int, dt: torch.dtype,
         rows, cols = Kd, R
         src = logical.transpose(1, 2)
     stride = rows * ld
+    if dt.itemsize == 2:
+        # 16-bit: filled and written in the storage type directly (the logical
+        # values are already rounded to it, so the conversion is exact)
+        buf = torch.full((batch, rows, ld), poison, dtype=dt)
+        buf[:, :, :cols] = src.to(dt)
+        return buf.reshape(-1), stride
     buf = torch.full((batch, rows, ld), poison, dtype=torch.float32)
     buf[:, :, :cols] = src
     return buf.to(dt).reshape(-1).contiguous(), stride

@@ -147,6 +147,19 @@ def test_k_zero_writes_zeros_and_empty_is_noop():
     assert torch.all(C == 7.0)
 
 
+@pytest.mark.parametrize("M,N,K,batch,am,bm,dist", [
+    (1, 1, 65536, 1, K_MAJOR, MN_MAJOR, "int"),         # one output, 1024 K blocks, exact
+    (3, 5, 16384, 1, MN_MAJOR, K_MAJOR, "uniform"),      # long K, ragged everything
+    (262144, 16, 32, 1, K_MAJOR, MN_MAJOR, "uniform"),   # 2048 row tiles, one ragged column block
+    (16, 131072, 64, 1, K_MAJOR, MN_MAJOR, "uniform"),   # 512 column tiles of 256
+    (8, 8, 8, 4096, K_MAJOR, K_MAJOR, "uniform"),        # 4096 batch entries of one tile each
+])
+def test_extreme_shapes(M, N, K, batch, am, bm, dist):
+    p = make_problem(M, N, K, a_major=am, b_major=bm, batch=batch, dist=dist, seed=M + N + K,
+                     out_dtype="f32")
+    _full(p, exact=dist == "int")
+
+
 def test_batched_small():
     for am, bm in MAJORS:
         p = make_problem(130, 200, 96, a_major=am, b_major=bm, batch=5, dist="normal",
@@ -287,6 +300,21 @@ def test_config_8192_integer_bit_exact():
     gpu = run_gpu(p)
     bi, mi, ni = sample_positions(p, 4000)
     check(p, gpu[bi, mi, ni], oracle_sampled(p, bi, mi, ni), exact=True)
+
+
+@pytest.mark.parametrize("am,extra", [(K_MAJOR, 160000), (MN_MAJOR, 2600000)])
+def test_operand_offsets_past_2_gib(am, extra):
+    """Leading dimensions padded so that the operands span more than 2^31
+    bytes (A, and with the M-major A also B): element offsets and the TMA
+    maps' byte strides pass the 32-bit range.  Sampled outputs vs the oracle;
+    about a fifth of the samples (K-major A: rows >= 6690) read A past 2^31."""
+    p = make_problem(8192, 256, 512, a_major=am, b_major=MN_MAJOR, dist="uniform", seed=31,
+                     out_dtype="bf16", ld_extra=extra)
+    assert p.A.numel() * p.A.element_size() > 2**31
+    gpu = run_gpu(p)
+    bi, mi, ni = sample_positions(p, 3000)
+    check(p, gpu[bi, mi, ni], oracle_sampled(p, bi, mi, ni))
+    assert np.all(np.isfinite(gpu))
 
 
 def test_config_skinny():
