@@ -35,7 +35,17 @@
  *   Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  No
  *   entry point except gemm_check synchronises.
  *   Allocation: the library allocates one 4-byte error word per device on its
- *   first launch there and nothing per call.
+ *   first launch there.  A launch that splits tiles along K (stream-K: chosen
+ *   automatically only for CTA-pair tiles whose last wave leaves every
+ *   cluster a long share of K, or forced with SMO_GEMM_STREAM_K=1) also uses
+ *   one workspace per (device, stream): an fp32 partial slot per cluster
+ *   (clusters x tile rows x tile columns x 4 bytes; 76 x 256 x 256 x 4 =
+ *   19.9 MB on a 152-SM GPU) and a counter per cluster.  It is allocated on
+ *   the first split launch on that stream, grown when a larger one is needed,
+ *   and kept until the process exits; while the stream is being captured into
+ *   a CUDA graph nothing is allocated and a launch without a large enough
+ *   workspace does not split.  Nothing else is allocated per call
+ *   (gemm_ex_noalloc allocates nothing at all).
  *   Errors: every entry point returns GEMM_OK (0) or a negative gemm_status_t;
  *   argument errors launch nothing and leave C untouched.
  */
