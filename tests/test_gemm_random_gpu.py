@@ -17,7 +17,7 @@ from tests.gemm_check import check, oracle_full, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 120
+N_CASES = 200
 
 
 @pytest.fixture(scope="module", autouse=True)
