@@ -340,23 +340,44 @@ def run_ours(args, world, rank, local):
     ev = [(timing_event(), timing_event()) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    graph = None
+    graph = graph_flush = None
+    f_start = torch.cuda.Event(enable_timing=True)
+    f_end = torch.cuda.Event(enable_timing=True)
     if args.graph:
-        # launch-bound shapes: the K launches (and their event pairs) replayed
-        # from one CUDA graph, so host call overhead is not in the device time
+        # launch-bound shapes: the K launches replayed from one CUDA graph, so
+        # host call overhead is not in the device time.  With L2 flushes the
+        # graph holds K (flush, launch) pairs and a second graph the K flushes
+        # alone; a step is the difference over K, each graph timed by one
+        # event pair (an event pair per launch would add its own few
+        # microseconds to every launch).  Without flushes, a launch event pair
+        # each.
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(args.steps):
                 if flush is not None:
                     flush.zero_()
-                ev[i][0].record(stream)
+                else:
+                    ev[i][0].record(stream)
                 launch()
-                ev[i][1].record(stream)
+                if flush is None:
+                    ev[i][1].record(stream)
+        if flush is not None:
+            graph_flush = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_flush, stream=stream):
+                for i in range(args.steps):
+                    flush.zero_()
         with torch.cuda.stream(stream):
             graph.replay()
+            if graph_flush is not None:
+                graph_flush.replay()
         torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
+    if graph_flush is not None:
+        with torch.cuda.stream(stream):
+            f_start.record(stream)
+            graph_flush.replay()
+            f_end.record(stream)
     t_start.record(stream)
     if graph is not None:
         with torch.cuda.stream(stream):
@@ -372,10 +393,15 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     clocks = sampler.stop()
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
-    # with L2 flushes between launches a step is the launch itself (sum of the
-    # launch event pairs); otherwise the whole timed region
-    total_s = (sum(launch_ms) if flush is not None else t_start.elapsed_time(t_end)) / 1e3
+    if graph_flush is not None:
+        # (flush, launch) pairs minus the flushes alone
+        total_s = (t_start.elapsed_time(t_end) - f_start.elapsed_time(f_end)) / 1e3
+        launch_ms = [total_s * 1e3 / args.steps] * args.steps
+    else:
+        launch_ms = [a.elapsed_time(b) for a, b in ev]
+        # with L2 flushes between launches a step is the launch itself (sum of
+        # the launch event pairs); otherwise the whole timed region
+        total_s = (sum(launch_ms) if flush is not None else t_start.elapsed_time(t_end)) / 1e3
     st = smo.gemm_check(stream)
     if st != smo.GEMM_OK:
         raise RuntimeError(smo.gemm_status_string(st))
@@ -490,7 +516,10 @@ def run_ours(args, world, rank, local):
                    "a_major": "M" if p.a_major else "K", "b_major": "N" if p.b_major else "K",
                    "in": p.in_dtype, "accumulate": "f32", "out": p.out_dtype,
                    "dist": p.dist, "seed": p.seed, "parallelism": f"replicas{world}",
-                   "l2": ("flushed before every launch (256 MiB memset between the launch event "
+                   "l2": ("flushed before every launch (256 MiB memset); a step is (a graph of K "
+                          "flush + launch pairs minus a graph of the K flushes) / K"
+                          if graph_flush is not None else
+                          "flushed before every launch (256 MiB memset between the launch event "
                           "pairs; steps timed by those pairs)") if flush is not None else
                          "no flush: A+B+C larger than twice the 129 MB L2",
                    "launch": "cuda graph replay" if args.graph else "back-to-back host launches",
