@@ -328,16 +328,12 @@ def run_ours(args, world, rank, local):
     time.sleep(0.3)
     # Inputs + output larger than twice the 129 MB L2 stream from HBM anyway;
     # smaller working sets get L2 flushed (256 MiB written) before every launch,
-    # outside the per-launch event pair.
+    # and the flush's time is kept out of the step (see the timing below).
     work_bytes = (p.A.numel() + p.B.numel()) * p.A.element_size() + C.numel() * C.element_size()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if work_bytes < (258 << 20) else None
-    def timing_event():
-        # events recorded inside a CUDA graph need the "external" record flag to be timed
-        if args.graph:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        return torch.cuda.Event(enable_timing=True)
-
-    ev = [(timing_event(), timing_event()) for _ in range(args.steps)]
+    # per-launch event pairs only where flushes sit between host launches
+    ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)] if flush is not None and not args.graph else [])
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     graph = graph_flush = None
@@ -349,18 +345,13 @@ def run_ours(args, world, rank, local):
         # graph holds K (flush, launch) pairs and a second graph the K flushes
         # alone; a step is the difference over K, each graph timed by one
         # event pair (an event pair per launch would add its own few
-        # microseconds to every launch).  Without flushes, a launch event pair
-        # each.
+        # microseconds to every launch).
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(args.steps):
                 if flush is not None:
                     flush.zero_()
-                else:
-                    ev[i][0].record(stream)
                 launch()
-                if flush is None:
-                    ev[i][1].record(stream)
         if flush is not None:
             graph_flush = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph_flush, stream=stream):
@@ -382,13 +373,18 @@ def run_ours(args, world, rank, local):
     if graph is not None:
         with torch.cuda.stream(stream):
             graph.replay()
-    else:
+    elif flush is not None:
         for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
+            flush.zero_()
             ev[i][0].record(stream)
             launch()
             ev[i][1].record(stream)
+    else:
+        # back to back with nothing between the launches: an event record
+        # between two kernels would add its own latency and keep the next
+        # launch's prologue from overlapping (programmatic dependent launch)
+        for i in range(args.steps):
+            launch()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -396,12 +392,15 @@ def run_ours(args, world, rank, local):
     if graph_flush is not None:
         # (flush, launch) pairs minus the flushes alone
         total_s = (t_start.elapsed_time(t_end) - f_start.elapsed_time(f_end)) / 1e3
-        launch_ms = [total_s * 1e3 / args.steps] * args.steps
-    else:
+        launch_ms = None
+    elif flush is not None:
+        # host launches with L2 flushes: a step is the launch itself, the sum
+        # of the launch event pairs (an upper bound: each pair adds a few us)
         launch_ms = [a.elapsed_time(b) for a, b in ev]
-        # with L2 flushes between launches a step is the launch itself (sum of
-        # the launch event pairs); otherwise the whole timed region
-        total_s = (sum(launch_ms) if flush is not None else t_start.elapsed_time(t_end)) / 1e3
+        total_s = sum(launch_ms) / 1e3
+    else:
+        total_s = t_start.elapsed_time(t_end) / 1e3
+        launch_ms = None
     st = smo.gemm_check(stream)
     if st != smo.GEMM_OK:
         raise RuntimeError(smo.gemm_status_string(st))
@@ -475,7 +474,7 @@ def run_ours(args, world, rank, local):
         return 0
 
     peaks, peak_src = load_peaks()
-    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    avg_launch_s = total_s / args.steps
     achieved = p.flops / avg_launch_s / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -493,8 +492,10 @@ def run_ours(args, world, rank, local):
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": peak_note,
                 "frac_of_sustained": achieved / peak_sus, "algorithmic_bytes": alg_bytes,
-                "kernel": KERNEL_NAME, "launch_ms_median": statistics.median(launch_ms),
-                "launch_ms_best": min(launch_ms)}
+                "kernel": KERNEL_NAME, "launch_ms_mean": avg_launch_s * 1e3}
+    if launch_ms:
+        roofline["launch_ms_median"] = statistics.median(launch_ms)
+        roofline["launch_ms_best"] = min(launch_ms)
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
