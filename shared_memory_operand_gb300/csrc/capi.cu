@@ -307,17 +307,19 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     if (stream_k != 0) {
         const int64_t waves = pl.tiles / maxc;
         const int64_t sk_tiles = pl.tiles - waves * maxc;
-        // Each split piece moves a 256 KiB (wide tiles: 512 KiB) fp32 partial through L2 (about
-        // 20 MB per launch for 76 clusters); measured on GB300 that costs more
-        // than the idle tail it removes unless every cluster's share of the
-        // split tiles is long.  Automatic: at least 48 K blocks per cluster.
-        // Wide tiles (512 KiB partials) lost 3.5% at 8192^3: automatic only on 256 x 256 tiles.
+        // Each split piece writes a 256 KiB (wide tiles: 512 KiB) fp32 partial
+        // and its owner reads it back; measured on GB300 the round trip of a
+        // CTA's half takes about 11 us (an SM moves 40-50 GB/s to and from L2),
+        // 18 K blocks of a wide tile's main loop.  That is more than the idle
+        // tail it removes unless every cluster's share of the split tiles is
+        // long.  Automatic: 256 x 256 tiles with at least 48 K blocks per
+        // cluster (wide tiles lost 3.5% at 8192^3 and 6% at 4096^3).
         const bool worth = stream_k == 1 || (!pl.wide && (sk_tiles * (int64_t)pl.num_k) / maxc >= 48);
-        // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
         // The owner streams the partials through the idle operand ring
         // (kFixRingBytes) in blocks of 128 accumulator columns.
         const bool fits = (size_t)pl.stages * pl.stage_stride >= smo::kFixRingBytes &&
                           pl.BN % (32 * smo::kFixChunks) == 0;
+        // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
         if (worth && fits && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
             const size_t work_bytes = (size_t)maxc * (size_t)pl.tile_m * (size_t)pl.BN * sizeof(float);
             // The stream's workspace is looked up and grown under the lock, so
