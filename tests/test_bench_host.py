@@ -1,13 +1,19 @@
 """Host logic of bench.py without a GPU: the multi-rank aggregation (max over
 ranks, whole-job throughput) on two gloo ranks, clock parsing, and the JSON
-contract of the reference arm's helpers."""
+contract of the reference arm (run whole, on one rank and under a two-rank
+torchrun: it times the oracle on the host and needs no GPU)."""
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch.multiprocessing as mp
 
 import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _free_port():
@@ -101,3 +107,38 @@ def test_bank_conflicts_from_profile(tmp_path, monkeypatch):
     assert bench.profiled_traffic("w") == 1e6
     (csrc / "k.cu").write_text("kernel v2")
     assert bench.profiled_bank_conflicts("w") is None
+
+
+def _json_lines(out: str):
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_single_rank():
+    """`bench.py --impl reference` times the oracle on the host (no GPU needed)
+    and prints one JSON line carrying the contract's keys."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3", "--workload", "gemm_256_bf16_f32"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    d = lines[0]
+    assert d["impl"] == "reference" and d["metric"] == "BF16 GEMM TFLOP/s" and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["steps"] == 3 and d["warmup"] == 3
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_two_ranks_prints_once():
+    """Under torchrun with two ranks only rank 0 runs and prints; both exit 0."""
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port),
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "3",
+                        "--warmup", "3", "--workload", "gemm_256_bf16_f32"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["impl"] == "reference"
