@@ -144,8 +144,8 @@ int gemm_debug_inject_stall(int on);
 
 /*
  * gemm_ex_noalloc: gemm_ex for callers that cannot allocate device memory.
- * The paper has no counterpart of this entry point; it exists for users of
- * this library, not for the method.
+ * None of the source pages describes such an entry point; it exists for
+ * users of this library, not for the method.
  *
  * Who needs it: callers whose device memory is owned entirely by a pool or
  * arena allocator (framework caching allocators, inference runtimes that hand
