@@ -1,7 +1,9 @@
 // Device pieces shared by the one-CTA and CTA-pair GEMM kernels: error
-// reporting, tile decoding and the epilogue (tensor memory -> registers ->
-// 128-byte-swizzled shared-memory slab -> TMA store, ragged row tails stored
-// directly).
+// reporting, tile decoding, the producer's per-lane TMA load slots, the
+// stream-K work split (whole tiles, then K ranges of the last wave's tiles),
+// its fp32 partials and their fix-up, and the epilogue (tensor memory ->
+// registers -> 128-byte-swizzled shared-memory slab -> TMA store, ragged row
+// tails stored directly).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>

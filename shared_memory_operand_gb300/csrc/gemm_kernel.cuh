@@ -1,10 +1,14 @@
-// Persistent, warp-specialised BF16/F16 GEMM for sm_103a (GB300).
+// Persistent, warp-specialised GEMM for sm_103a (GB300), one CTA per
+// 128 x BN output tile: bf16 / f16 operands (tcgen05.mma kind::f16) or FP8
+// E4M3 / E5M2 operands (kind::f8f6f4), fp32 accumulation.
 //
-//   warp 0 (one thread)  TMA producer: fills a ring of `stages` shared-memory
-//                        stages with 128-byte-swizzled A and B tiles
-//                        (cp.async.bulk.tensor, mbarrier complete_tx), handed
-//                        over in groups of `kgroup` stages per barrier pair.
-//   warp 1 (one thread)  MMA issuer: 4 x tcgen05.mma (128 x BN x 16) per stage,
+//   warp 0               TMA producer: lane 0 waits for a free group of
+//                        stages and arms its barrier; lanes 0 .. n-1 then
+//                        issue the group's loads of 128-byte-swizzled A and B
+//                        tiles together (cp.async.bulk.tensor, mbarrier
+//                        complete_tx), `kgroup` stages per barrier pair.
+//   warp 1 (one thread)  MMA issuer: 4 x tcgen05.mma (128 x BN x 32 bytes of
+//                        K: K = 16 for 16-bit, 32 for FP8) per stage,
 //                        accumulating in tensor memory; tcgen05.commit frees
 //                        the group (split barrier) and, after the last K block,
 //                        publishes the accumulator.
