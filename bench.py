@@ -401,6 +401,25 @@ def run_ours(args, world, rank, local):
     else:
         total_s = t_start.elapsed_time(t_end) / 1e3
         launch_ms = None
+    # Per-launch statistics (median, best) from a separate sample after the
+    # timed region: an event pair around each of up to 100 launches (each pair
+    # adds a few us, so these read slightly long); not used for `value`.
+    launch_sample = None
+    if launch_ms is None:
+        n_s = min(args.steps, 100)
+        ev_s = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_s)]
+        with torch.cuda.stream(stream):
+            for a, b in ev_s:
+                if flush is not None:
+                    flush.zero_()
+                a.record(stream)
+                launch()
+                b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = [a.elapsed_time(b) for a, b in ev_s]
+        launch_sample = {"launches": n_s, "median_ms": statistics.median(ms), "best_ms": min(ms),
+                         "how": "event pair around each launch, after the timed region and a pause "
+                                "(the power limiter has recovered: burst, not settled, rate)"}
     st = smo.gemm_check(stream)
     if st != smo.GEMM_OK:
         raise RuntimeError(smo.gemm_status_string(st))
@@ -496,6 +515,8 @@ def run_ours(args, world, rank, local):
     if launch_ms:
         roofline["launch_ms_median"] = statistics.median(launch_ms)
         roofline["launch_ms_best"] = min(launch_ms)
+    if launch_sample:
+        roofline["launch_sample"] = launch_sample
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
