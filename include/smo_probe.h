@@ -1,15 +1,20 @@
 /*
- * smo_probe.h -- shared-memory bank microbenchmark exported by libsmo_gemm.so
+ * smo_probe.h -- measurement probes exported by libsmo_gemm.so: the
+ * shared-memory bank microbenchmark, the tensor-core issue-rate probe and the
+ * global-to-shared bandwidth probe.
  *
- * A measurement tool beside the GEMM, not part of it.  It times one shared
- * memory access pattern in isolation so that the bank-conflict degree a
- * simulator predicts for that pattern can be checked on the hardware (method:
+ * Measurement tools beside the GEMM, not part of it.  The bank microbenchmark
+ * times one shared-memory access pattern in isolation so that the
+ * bank-conflict degree a simulator predicts for that pattern can be checked
+ * on the hardware (method:
  * "A Deep Dive into LDS Optimizations on AMD Instinct MI450 GPUs", "Measuring
  * It: An LDS Bandwidth Microbenchmark", and the padding measurement of the
  * "LDS Optimization" skill page, "Padding Amount").
  */
 #ifndef SMO_PROBE_H
 #define SMO_PROBE_H
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -46,6 +51,24 @@ int smem_bank_probe(const void* offsets, int access_bytes, int is_store, int ite
  * number of clusters launched, or a negative value on error.  Asynchronous.
  */
 int tc_peak_probe(int iters, void* out, int max_clusters, void* stream);
+
+/*
+ * l2_read_probe: global-to-shared-memory bandwidth probe.  Launches up to
+ * max_ctas CTAs (at most one per SM) on `stream`; each streams `iters` blocks
+ * of 32 KiB of the device buffer `src` (`bytes` long, 16-byte aligned,
+ * caller-owned, only read) into a ring of `stages` (1..6) shared-memory
+ * stages with untiled bulk copies (cp.async.bulk, mbarrier completion), all
+ * of them in flight, and nothing else.  CTA c reads blocks c, c + ctas, c + 2 ctas, ... modulo
+ * bytes / 32 KiB.  A buffer that fits in L2 (after one warm-up launch)
+ * measures the rate at which L2 feeds the SMs -- the path of the GEMM's
+ * operand loads; a buffer several times the L2 size measures the HBM-fed rate.
+ * out: device pointer to 2 * max_ctas int64, per CTA [clock64 cycles,
+ * global-timer ns] of its copy loop (-1 if a bounded wait ran out).
+ * Bytes moved: ctas * iters * 32768.  Returns the number of CTAs launched, or
+ * -1 (bad argument), -2 (misaligned src), -4 (launch failed).  Asynchronous.
+ */
+int l2_read_probe(const void* src, size_t bytes, int iters, int stages, void* out, int max_ctas,
+                  void* stream);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,8 @@ DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32, "e4m3": GEMM
 
 # Every symbol include/smo_gemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_ex", "gemm_check", "gemm_status_string", "gemm_set_timeout_ns",
-           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "smem_bank_probe", "tc_peak_probe")
+           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "smem_bank_probe", "tc_peak_probe",
+           "l2_read_probe")
 
 
 class GemmError(RuntimeError):
@@ -62,6 +63,8 @@ def load_library(path: str = LIB_PATH, build: bool = False) -> ctypes.CDLL:
     L.smem_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
     L.tc_peak_probe.restype = i32
     L.tc_peak_probe.argtypes = [i32, vp, i32, vp]
+    L.l2_read_probe.restype = i32
+    L.l2_read_probe.argtypes = [vp, ctypes.c_size_t, i32, i32, vp, i32, vp]
     L.gemm_check.restype = i32
     L.gemm_check.argtypes = [vp]
     L.gemm_status_string.restype = ctypes.c_char_p
@@ -176,6 +179,16 @@ def smem_bank_probe(offsets, access_bytes: int, is_store: bool, iters: int, cycl
                                         _ptr(cycles_out), _stream(stream))
     if st != 0:
         raise RuntimeError(f"smem_bank_probe failed: {st}")
+
+
+def l2_read_probe(src, nbytes: int, iters: int, out, max_ctas: int = 1 << 20, stages: int = 6,
+                  stream=None) -> int:
+    """Global-to-shared bandwidth probe (see include/smo_probe.h); returns CTAs."""
+    n = load_library().l2_read_probe(_ptr(src), int(nbytes), int(iters), int(stages), _ptr(out),
+                                     int(max_ctas), _stream(stream))
+    if n < 1:
+        raise RuntimeError(f"l2_read_probe failed: {n}")
+    return int(n)
 
 
 def tc_peak_probe(iters: int, out, max_clusters: int = 1 << 20, stream=None) -> int:

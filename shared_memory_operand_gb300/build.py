@@ -20,7 +20,7 @@ CUDA_HOME = os.environ.get("CUDA_HOME", "/usr/local/cuda")
 NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 GENCODE = "arch=compute_103a,code=sm_103a"
 
-SOURCES_CU = ["capi.cu", "smem_probe.cu", "tc_probe.cu"]
+SOURCES_CU = ["capi.cu", "smem_probe.cu", "tc_probe.cu", "l2_probe.cu"]
 SOURCES_CPP = ["planner.cpp"]
 HEADERS = ["gemm_kernel.cuh", "gemm_kernel_pair.cuh", "gemm_common.cuh", "ptx.cuh", "gemm_params.h", "planner.h"]
 

@@ -87,3 +87,39 @@ def test_tensor_peak_probe_runs_on_every_cluster():
     flops = n * iters * 4 * 2.0 * 256 * 256 * 16
     tflops = flops / (e0.elapsed_time(e1) / 1e3) / 1e12
     assert tflops > 300.0, tflops
+
+
+def _l2_rate(buf, iters, stages=6):
+    out = torch.full((2 * 1024,), -2, dtype=torch.int64, device="cuda")
+    smo.l2_read_probe(buf, buf.numel(), 50, out, 1024, stages)  # warm (and bring an L2-sized buffer in)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    n = smo.l2_read_probe(buf, buf.numel(), iters, out, 1024, stages)
+    e1.record()
+    torch.cuda.synchronize()
+    per = out[: 2 * n].view(n, 2).cpu()
+    assert n >= 1 and torch.all(per[:, 0] > 0) and torch.all(per[:, 1] > 0), "a bounded wait ran out"
+    return n * iters * 32768 / (e0.elapsed_time(e1) / 1e3)
+
+
+def test_l2_read_probe_runs_and_l2_outpaces_hbm():
+    """Bulk copies from global into shared memory on every SM, nothing else:
+    every CTA finishes within its bounded waits; a 64 MiB buffer (resident in
+    the 126 MB L2) streams faster than a 2 GiB one (from HBM), and the HBM rate
+    is of the order of the measured copy bandwidth."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    smo.load_library(build=True)
+    small = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+    big = torch.zeros(2 << 30, dtype=torch.uint8, device="cuda")
+    l2 = _l2_rate(small, 2000)
+    hbm = _l2_rate(big, 400)
+    print(f"L2 -> SM {l2 / 1e12:.2f} TB/s, HBM -> SM {hbm / 1e12:.2f} TB/s")
+    assert l2 > hbm > 2e12, (l2, hbm)
+    # fewer copies in flight per SM, lower rate (Little's law: rate = bytes in flight / latency)
+    by_stages = {s: _l2_rate(small, 1000, s) for s in (1, 2, 4, 6)}
+    print("L2 -> SM by 32 KiB stages in flight:", {s: round(r / 1e12, 2) for s, r in by_stages.items()})
+    assert by_stages[1] < by_stages[2] < by_stages[6], by_stages
+    with pytest.raises(RuntimeError):
+        smo.l2_read_probe(small[1:], 1 << 20, 10, torch.zeros(8, dtype=torch.int64, device="cuda"), 1)
