@@ -62,7 +62,7 @@ def kernel_source_hash(csrc: str = None) -> str:
     h = hashlib.sha256()
     csrc = csrc or os.path.join(ROOT, "shared_memory_operand_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.startswith("smem_probe") or name.startswith("tc_probe"):
+        if name.startswith(("smem_probe", "tc_probe", "l2_probe")):
             continue
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
