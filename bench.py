@@ -82,7 +82,7 @@ def profiled_counters(workload: str) -> dict:
     if not src or src.group(1) != kernel_source_hash():
         return {}
     return {m.group(1): float(m.group(2))
-            for m in re.finditer(r"^([a-z_]+):\s*([0-9][0-9.eE+]*)\s*$", text, re.M)}
+            for m in re.finditer(r"^([a-z][a-z0-9_]*):\s*([0-9][0-9.eE+]*)\s*$", text, re.M)}
 
 
 def profiled_traffic(workload: str):
@@ -319,6 +319,25 @@ def run_ours(args, world, rank, local):
                    "clusters": ncl, "what": "tcgen05.mma.cta_group::2 256x256x16 bf16 back to back on "
                                             "resident smem tiles, no loads (smo_probe.h tc_peak_probe)"}
 
+    # global-to-shared bandwidth probe: bulk copies of an L2-resident 64 MiB
+    # buffer into shared memory on every SM, no compute
+    l2_probe = None
+    if rank == 0:
+        pbuf = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
+        pout = torch.zeros(2 * 1024, dtype=torch.int64, device=dev)
+        smo.l2_read_probe(pbuf, pbuf.numel(), 50, pout, 1024, stream=stream)   # warm, fills L2
+        le0, le1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l2_iters = 1500
+        le0.record(stream)
+        nct = smo.l2_read_probe(pbuf, pbuf.numel(), l2_iters, pout, 1024, stream=stream)
+        le1.record(stream)
+        torch.cuda.synchronize(dev)
+        l2_probe = {"value": nct * l2_iters * 32768 / (le0.elapsed_time(le1) / 1e3) / 1e9, "unit": "GB/s",
+                    "ctas": nct, "buffer_mib": 64,
+                    "what": "cp.async.bulk 32 KiB copies of an L2-resident buffer into 6 shared-memory stages "
+                            "on every SM, no compute (smo_probe.h l2_read_probe)"}
+        del pbuf, pout
+
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize(dev)
@@ -517,6 +536,14 @@ def run_ours(args, world, rank, local):
         roofline["launch_ms_best"] = min(launch_ms)
     if launch_sample:
         roofline["launch_sample"] = launch_sample
+    # the operand stream from L2 into shared memory (bytes from the committed
+    # ncu summary, hash-matched) against the probe's rate
+    l2b = profiled_counters(args.workload).get("l2_to_sm_bytes_per_launch")
+    if l2b and l2_probe:
+        ach = l2b / avg_launch_s / 1e9
+        roofline["l2_to_sm"] = {"achieved": ach, "peak": l2_probe["value"], "unit": "GB/s",
+                                "frac": ach / l2_probe["value"], "bytes_per_launch": int(l2b),
+                                "peak_source": "l2_to_sm_probe of this run"}
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -553,6 +580,7 @@ def run_ours(args, world, rank, local):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "tensor_peak_probe": tc_peak,
+        "l2_to_sm_probe": l2_probe,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -99,12 +99,13 @@ def test_bank_conflicts_from_profile(tmp_path, monkeypatch):
     (prof / f"{bench.KERNEL_NAME}_w.md").write_text(
         f"# title\n\nkernel_source_hash: {h}\ndram_bytes_per_launch: 1e6\nsmem_st_requests: 1000\n"
         "smem_st_bank_conflicts: 50\nsmem_ld_requests: 10\nsmem_ld_bank_conflicts: 0\n"
-        "smem_excess_wavefronts: 0\n\n| table | 12 |\n")
+        "smem_excess_wavefronts: 0\nl2_to_sm_bytes_per_launch: 4096\n\n| table | 12 |\n")
     c = bench.profiled_bank_conflicts("w")
     assert c["st_per_request"] == pytest.approx(0.05)
     assert c["ld_per_request"] == 0.0
     assert c["excess_wavefronts"] == 0 and c["st_requests"] == 1000
     assert bench.profiled_traffic("w") == 1e6
+    assert bench.profiled_counters("w")["l2_to_sm_bytes_per_launch"] == 4096
     (csrc / "k.cu").write_text("kernel v2")
     assert bench.profiled_bank_conflicts("w") is None
 
