@@ -14,7 +14,10 @@ section "A Linear Layout Refresher":
 and section "Lowering local_load to ds_load_tr in Triton":
   * cvt = dstLL.invertAndCompose(sharedLL) maps each destination hardware
     position to the shared offset that holds the same coordinates; sharedLL
-    must be surjective for the lookup to succeed.
+    must be surjective for the lookup to succeed;
+  * the same section's address computation inverts the full tile's shared
+    layout (coordinates -> offset) before composing it with the repetition
+    layout: ``invert`` below (bijective layouts with one input dimension).
 
 Representation: ``ins`` is an ordered list of (input name, [basis images]);
 each image is a tuple with one integer per output dimension.  ``outs`` is an

@@ -7,7 +7,7 @@ from math import gcd
 import pytest
 
 from oracle import banksim
-from oracle.f2 import LinearLayout, divide_left, identity_1d
+from oracle.f2 import LinearLayout, divide_left, enumerate_map, identity_1d
 
 
 def _parse_layouts(path):
@@ -269,3 +269,67 @@ def test_tma_box_layout_equals_canonical_umma_layout(mn_major):
             assert a == b
             offs.add(a)
     assert offs == set(range(0, tile_mn * 128, 2))
+
+
+# ------------------------------------------------------------- invert
+def test_invert_against_worked_cvt_table(mi450):
+    """MI450 post, "Lowering local_load to ds_load_tr in Triton": the address
+    step inverts the shared layout (offset -> [M, K]) and composes the result
+    with the destination layout.  shared^-1 applied to each basis image of
+    dstLL must give the printed cvt table, and shared^-1 must undo shared on
+    every offset (brute force over the whole tile)."""
+    L, _ = mi450
+    dst = _mk(L["dst"], ["register", "lane"], [("M", 32), ("K", 8)])
+    shared = _mk(L["shared"], ["offset"], [("M", 32), ("K", 8)])
+    want = _mk(L["cvt"], ["register", "lane"], [("offset", 256)])
+    inv = shared.invert()
+    assert inv.in_names() == ["M", "K"] and inv.outs == [("offset", 256)]
+    for dim in ("register", "lane"):
+        got = [inv.apply(M=m, K=k) for (m, k) in dst.bases(dim)]
+        assert got == want.bases(dim)
+    seen = 0
+    for ins, img in enumerate_map(shared):
+        assert inv.apply(M=img[0], K=img[1]) == (ins["offset"],)
+        seen += 1
+    assert seen == 256
+
+
+def test_invert_round_trip_on_swizzled_and_microbenchmark_layouts(mi450):
+    """A 128-byte XOR swizzle in 16-byte units (offset chunk bits -> column,
+    row bits -> row and column): its matrix is not a permutation, so a
+    transpose in place of the inverse, or a dropped XOR term, fails the round
+    trip.  Also the microbenchmark's plain [4, 256] layout."""
+    L, _ = mi450
+    sw = LinearLayout([("offset", [(0, 1), (0, 2), (0, 4), (1, 1), (2, 2), (4, 4)])],
+                      [("row", 8), ("col", 8)])
+    plain = _mk(L["mb_plain"], ["offset"], [("d0", 4), ("d1", 256)])
+    for lay, names in ((sw, ("row", "col")), (plain, ("d0", "d1"))):
+        inv = lay.invert()
+        n = 0
+        for ins, img in enumerate_map(lay):
+            assert inv.apply(**dict(zip(names, img))) == (ins["offset"],)
+            n += 1
+        assert n == lay.in_size("offset")
+        # and the other way round: lay(inv(x)) == x on every output coordinate
+        for a in range(lay.out_size(names[0])):
+            for b in range(lay.out_size(names[1])):
+                (off,) = inv.apply(**{names[0]: a, names[1]: b})
+                assert lay.apply(offset=off) == (a, b)
+    # by hand: row bit i alone is offset bits (3 + i) and i (the XOR cancels
+    # the column term); column bit i is offset bit i
+    inv = sw.invert()
+    assert inv.bases("row") == [(9,), (18,), (36,)]
+    assert inv.bases("col") == [(1,), (2,), (4,)]
+
+
+def test_invert_rejects_non_bijective_and_multi_input(mi450):
+    L, _ = mi450
+    part = _mk(L["mb_part"], ["offset", "partition"], [("d0", 4), ("d1", 256)])
+    with pytest.raises(ValueError):
+        part.invert()                         # two input dimensions
+    collapsed = LinearLayout([("offset", [(1, 0), (2, 0), (0, 1), (0, 1)])], [("M", 4), ("K", 4)])
+    with pytest.raises(ValueError):
+        collapsed.invert()                    # rank 3 of 4
+    short = LinearLayout([("offset", [(1, 0), (2, 0), (0, 1)])], [("M", 4), ("K", 4)])
+    with pytest.raises(ValueError):
+        short.invert()                        # injective, not surjective
