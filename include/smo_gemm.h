@@ -164,10 +164,12 @@ int gemm_debug_inject_stall(int on);
  * the array's device address once (cudaGetSymbolAddress); make that first call
  * before any stream capture.
  * Calls no cudaMalloc, cudaFree or other allocating routine.
- * Every call shares the array: each call clears the error word on `stream`
- * (cudaMemsetAsync) before its launch, so calls that overlap on the GPU race on
- * it.  A bounded-wait timeout of this variant is recorded only in that shared
- * word (gemm_check does not read it); C is then incomplete.
+ * Every call shares the array.  Its error word starts at zero on each device
+ * and is written only when a kernel's bounded wait runs out (first writer
+ * wins); it keeps that code, across later calls, until gemm_check_noalloc
+ * reads and clears it.  gemm_check does not read it.  Calls that overlap on
+ * the GPU race on the shared word: a reported timeout cannot be attributed to
+ * one of them, and C of each of them may be incomplete.
  */
 int gemm_ex_noalloc(const void* A, int64_t lda, int a_major,
                     const void* B, int64_t ldb, int b_major,
@@ -176,6 +178,20 @@ int gemm_ex_noalloc(const void* A, int64_t lda, int a_major,
                     int in_dtype, int out_dtype,
                     int64_t batch, int64_t strideA, int64_t strideB, int64_t strideC,
                     void* stream);
+
+/*
+ * gemm_check_noalloc: the error report of gemm_ex_noalloc, itself allocating
+ * nothing.  None of the source pages describes it; it belongs to the
+ * allocation-free entry point above.  Synchronises `stream`, then reads the
+ * static error word: GEMM_ERR_TIMEOUT if a gemm_ex_noalloc kernel's bounded
+ * wait ran out since the previous gemm_check_noalloc on this device (that
+ * kernel returned early and its C is incomplete; the word is cleared),
+ * GEMM_ERR_CUDA for a CUDA error, else GEMM_OK.  Reads and clears with
+ * synchronous cudaMemcpy / cudaMemset of the 4-byte word: call it outside
+ * stream capture.  Like gemm_ex_noalloc, its first call on a device resolves
+ * the array's address.
+ */
+int gemm_check_noalloc(void* stream);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,8 @@ DTYPE_CODES = {"bf16": GEMM_BF16, "f16": GEMM_F16, "f32": GEMM_F32, "e4m3": GEMM
 
 # Every symbol include/smo_gemm.h declares.
 EXPORTS = ("gemm_bf16", "gemm_ex", "gemm_check", "gemm_status_string", "gemm_set_timeout_ns",
-           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "smem_bank_probe", "tc_peak_probe",
+           "gemm_plan_describe", "gemm_debug_inject_stall", "gemm_ex_noalloc", "gemm_check_noalloc",
+           "smem_bank_probe", "tc_peak_probe",
            "l2_read_probe")
 
 
@@ -67,6 +68,8 @@ def load_library(path: str = LIB_PATH, build: bool = False) -> ctypes.CDLL:
     L.l2_read_probe.argtypes = [vp, ctypes.c_size_t, i32, i32, vp, i32, vp]
     L.gemm_check.restype = i32
     L.gemm_check.argtypes = [vp]
+    L.gemm_check_noalloc.restype = i32
+    L.gemm_check_noalloc.argtypes = [vp]
     L.gemm_status_string.restype = ctypes.c_char_p
     L.gemm_status_string.argtypes = [i32]
     L.gemm_set_timeout_ns.restype = i64
@@ -150,6 +153,11 @@ def gemm_ex_status(*args, **kw) -> int:
 
 def gemm_check(stream=None) -> int:
     return int(load_library().gemm_check(_stream(stream)))
+
+
+def gemm_check_noalloc(stream=None) -> int:
+    """Error report of gemm_ex_noalloc (synchronises; allocates nothing)."""
+    return int(load_library().gemm_check_noalloc(_stream(stream)))
 
 
 def gemm_set_timeout_ns(ns: int) -> int:

@@ -436,7 +436,10 @@ int noalloc_state(NoAllocState** out) {
         }
         void* ptr = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e == cudaSuccess && ptr != nullptr && major == 10 && minor == 3 && g_encode) {
+        // The error word starts at zero on this device (static storage is
+        // zero-initialised at module load; cleared again here explicitly).
+        if (e == cudaSuccess && ptr != nullptr && major == 10 && minor == 3 && g_encode &&
+            cudaMemset(ptr, 0, sizeof(int32_t)) == cudaSuccess) {
             n.scratch = static_cast<int32_t*>(ptr);
             n.ds.usable = true;
             n.usable = true;
@@ -637,15 +640,36 @@ int gemm_ex_noalloc(const void* A, int64_t lda, int a_major, const void* B, int6
     st = noalloc_state(&na);
     if (st != GEMM_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    // The shared array keeps the previous call's contents: the error word must
-    // start at zero for this launch (memset on the stream, no allocation).
-    if (K > 0 && cudaMemsetAsync(na->scratch, 0, sizeof(int32_t), stream) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
-    }
-    // stream-K would need a workspace: this entry point never splits tiles
+    // The shared error word is not cleared per call: the kernel only ever
+    // writes it (first writer wins) and gemm_check_noalloc reads and clears
+    // it, so a timeout stays visible until it has been reported, whatever
+    // calls follow it.  stream-K would need a workspace: this entry point
+    // never splits tiles.
     return run_gemm(na->ds, na->scratch, 0, A, lda, a_major, B, ldb, b_major, C, ldc, M, N, K, in_dtype,
                     out_dtype, batch, strideA, strideB, strideC, stream);
+}
+
+int gemm_check_noalloc(void* stream_) {
+    NoAllocState* na = nullptr;
+    int st = noalloc_state(&na);
+    if (st != GEMM_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int32_t h = 0;
+    if (cudaMemcpy(&h, na->scratch, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (h != 0) {
+        if (cudaMemset(na->scratch, 0, sizeof(int32_t)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
 }
 
 }  // extern "C"

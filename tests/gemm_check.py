@@ -29,9 +29,11 @@ def canary(dt: torch.dtype) -> torch.Tensor:
     return torch.tensor([0x7E5A], dtype=torch.int16).view(dt)
 
 
-def run_gpu(p, stream=None, device="cuda", fn=None):
-    """Copies the operands to the device, runs gemm_ex on a NaN-poisoned C with
-    canary guard bands, checks the guards, returns C (batch, M, N) as float64."""
+def run_gpu(p, stream=None, device="cuda", fn=None, check_fn=None):
+    """Copies the operands to the device, runs gemm_ex (or `fn`) on a
+    NaN-poisoned C with canary guard bands, asks gemm_check (or `check_fn`)
+    for the kernel's status, checks the guards, returns C (batch, M, N) as
+    float64."""
     A = p.A.to(device)
     B = p.B.to(device)
     odt = _TORCH_OUT[p.out_dtype]
@@ -43,7 +45,7 @@ def run_gpu(p, stream=None, device="cuda", fn=None):
     call(A, p.lda, p.a_major, B, p.ldb, p.b_major, C, p.ldc, p.M, p.N, p.K,
          in_dtype=p.in_dtype, out_dtype=p.out_dtype, batch=p.batch, strideA=p.strideA,
          strideB=p.strideB, strideC=p.strideC, stream=stream)
-    st = smo.gemm_check(stream)
+    st = (check_fn or smo.gemm_check)(stream)
     assert st == smo.GEMM_OK, smo.gemm_status_string(st)
     raw = buf.view(torch.int32 if odt == torch.float32 else torch.int16).cpu()
     can = canary(odt).view(torch.int32 if odt == torch.float32 else torch.int16)
@@ -95,25 +97,3 @@ def check(p, gpu: np.ndarray, ref64: np.ndarray, exact: bool = False) -> dict:
     fro_tol = {"f32": 1e-5, "bf16": 4e-3, "f16": 5e-4}[p.out_dtype]
     assert rel_fro <= fro_tol, f"relative Frobenius error {rel_fro} > {fro_tol}"
     return {"max_abs": float(err.max()) if err.size else 0.0, "rel_fro": rel_fro}
-
-
-def sample_positions(p, count: int, seed: int = 0):
-    """Random (batch, m, n) positions plus the four corners of every batch
-    entry's last tile row/column (ragged edges)."""
-    rng = np.random.default_rng(seed)
-    bi = rng.integers(0, p.batch, count)
-    mi = rng.integers(0, p.M, count)
-    ni = rng.integers(0, p.N, count)
-    extra = []
-    for b in {0, p.batch - 1}:
-        for m in {0, p.M - 1, (p.M - 1) // 128 * 128}:
-            for n in {0, p.N - 1, (p.N - 1) // 128 * 128}:
-                extra.append((b, m, n))
-    e = np.array(extra, dtype=np.int64)
-    return (np.concatenate([bi, e[:, 0]]), np.concatenate([mi, e[:, 1]]),
-            np.concatenate([ni, e[:, 2]]))
-
-
-def oracle_sampled(p, bi, mi, ni):
-    return og.gemm_f64_sampled(p.bits("A"), p.lda, p.a_major, p.bits("B"), p.ldb, p.b_major,
-                               p.in_dtype, p.K, bi, mi, ni, p.strideA, p.strideB)
