@@ -34,6 +34,7 @@ struct DevState {
     int num_sms = 0;
     int32_t* d_err = nullptr;
     bool attr_set[12] = {};         // one-CTA kernels: [(KIND * 3 + OUT) * 2 + KG - 1]
+    bool split_attr_set[4] = {};    // split-K one-CTA kernels (fp32 out): [KIND * 2 + KG - 1]
     bool pair_attr_set[12] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT]
     int pair_max_clusters[12] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
     // Stream-K workspace, one per stream so that GEMMs running concurrently
@@ -51,7 +52,7 @@ std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-using PlanKey = std::tuple<int64_t, int64_t, int64_t, int, int, int, int, int64_t, int, int>;
+using PlanKey = std::tuple<int64_t, int64_t, int64_t, int, int, int, int, int64_t, int, int, int>;
 std::map<PlanKey, Plan> g_plans;
 
 int elem_size(int dt) { return dt == GEMM_F32 ? 4 : (dt == GEMM_E4M3 || dt == GEMM_E5M2) ? 1 : 2; }
@@ -95,7 +96,15 @@ int force_bn_from_env() {
     const char* s = std::getenv("SMO_GEMM_FORCE_BN");
     if (!s) return 0;
     int v = std::atoi(s);
-    return (v == 128 || v == 256 || v == 512 || v == 1024) ? v : 0;
+    return (v == 128 || v == 192 || v == 256 || v == 384 || v == 512 || v == 1024) ? v : 0;
+}
+
+// Split-K policy of the one-CTA kernel: SMO_GEMM_SPLIT_K=0 never, =1 whenever
+// the plan allows it, unset = the planner's choice (tile-starved problems).
+int split_k_from_env() {
+    const char* s = std::getenv("SMO_GEMM_SPLIT_K");
+    if (!s) return -1;
+    return s[0] == '0' ? 0 : 1;
 }
 
 // Lazily initialises the per-device state of the current device.
@@ -152,12 +161,13 @@ int validate(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_d
 Plan cached_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype, int out_dtype,
                  int64_t batch, int num_sms) {
     int fbn = force_bn_from_env();
-    PlanKey key{M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn};
+    int split = split_k_from_env();
+    PlanKey key{M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn, split};
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) return it->second;
     if (g_plans.size() > 4096) g_plans.clear();
-    Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn);
+    Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn, split);
     g_plans[key] = p;
     return p;
 }
@@ -213,35 +223,40 @@ int encode_fused(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t 
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
 }
 
-template <int OUT, int KG, int KIND>
+template <int OUT, int KG, int KIND, int SPLIT>
 int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
                      const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
-    auto kern = smo::smo_gemm_kernel<OUT, KG, KIND>;
-    const int slot = (KIND * 3 + OUT) * 2 + KG - 1;
+    auto kern = smo::smo_gemm_kernel<OUT, KG, KIND, SPLIT>;
     {
         std::lock_guard<std::mutex> lk(g_mu);     // once per device and kernel variant
-        if (!ds.attr_set[slot]) {
+        bool& set = SPLIT ? ds.split_attr_set[KIND * 2 + KG - 1] : ds.attr_set[(KIND * 3 + OUT) * 2 + KG - 1];
+        if (!set) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
                 cudaSuccess) {
                 cudaGetLastError();
                 return GEMM_ERR_LAUNCH;
             }
-            ds.attr_set[slot] = true;
+            set = true;
         }
     }
     // programmatic stream serialization: the kernel's prologue may overlap the
-    // previous kernel's tail (the kernel waits for it before touching memory)
+    // previous kernel's tail (the kernel waits for it before touching memory);
+    // split-K: clusters of two CTAs, one cluster per tile
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
     cfg.blockDim = dim3(smo::kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = SPLIT ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, kp) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -252,8 +267,15 @@ int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const 
 template <int OUT, int KIND>
 int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
                   const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
-    return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND>(pl, ds, ta, tb, tc, kp, stream)
-                          : launch_single_kg<OUT, 1, KIND>(pl, ds, ta, tb, tc, kp, stream);
+    if constexpr (OUT == smo::OUT_F32) {
+        if (pl.split)
+            return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 1>(pl, ds, ta, tb, tc, kp, stream)
+                                  : launch_single_kg<OUT, 1, KIND, 1>(pl, ds, ta, tb, tc, kp, stream);
+    } else {
+        if (pl.split) return GEMM_ERR_UNSUPPORTED;     // the planner splits fp32 output only
+    }
+    return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 0>(pl, ds, ta, tb, tc, kp, stream)
+                          : launch_single_kg<OUT, 1, KIND, 0>(pl, ds, ta, tb, tc, kp, stream);
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM; the persistent grid is
@@ -616,7 +638,7 @@ int64_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, int a_major, int b_m
     int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
     if (st != GEMM_OK) return st;
     Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms > 0 ? num_sms : 1,
-                            force_bn_from_env());
+                            force_bn_from_env(), split_k_from_env());
     std::string s = smo::describe_json(p);
     if (buf && buflen > 0) {
         size_t n = s.size() < buflen - 1 ? s.size() : buflen - 1;

@@ -404,6 +404,92 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
     }
 }
 
+// Split-K epilogue of one warp (fp32 output; one tile per 2-CTA cluster, the
+// two CTAs holding the partial sums of the two halves of K).  The tile's
+// column chunks are shared out: CTA rank 0 owns chunks [0, h), rank 1 chunks
+// [h, epi_chunks), h = epi_chunks / 2.  Each CTA
+//   1. stores its own chunks' partial plainly (slab + TMA store);
+//   2. stages its partial of the peer's chunks in the idle operand ring;
+//   3. once its plain stores are complete, arrives (release, cluster scope)
+//      on the peer's `peer_bar`, every lane for its own direct stores;
+//   4. waits (acquire, cluster scope) until the peer's plain stores of those
+//      chunks are complete and adds its staged partial to them with TMA
+//      reduce-adds (fp32, rounded to nearest; ragged row tails by atomic
+//      adds).
+// Every output is then fl(p0 + p1) of the two partials: one rounding of two
+// addends, independent of which add came first, so the result is
+// deterministic.  `stage`: this warp's staging slots (up to 4 chunks of
+// kEpiSlabBytes).  Returns false if the wait for the peer ran out.
+template <typename Release>
+__device__ __forceinline__ bool epilogue_split_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
+                                                    uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
+                                                    int32_t m0, int32_t n0, int b, uint32_t rank, uint32_t stage,
+                                                    uint32_t peer_bar, uint32_t own_bar, int64_t budget,
+                                                    Release release) {
+    constexpr int kChunkCols = 32;                  // fp32: 32 columns per 128-byte chunk
+    const int h = p.epi_chunks / 2;
+    const int own0 = rank ? h : 0, own1 = rank ? p.epi_chunks : h;
+    const int oth0 = rank ? 0 : h, oth1 = rank ? h : p.epi_chunks;
+    for (int c = own0; c < own1; ++c) {
+        const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
+        if (lane == 0) bulk_wait_read<1>();         // this slab's previous store has read it
+        __syncwarp();
+        uint32_t v[32];
+        epi_load_chunk<OUT_F32>(tmem_acc, lane_field, c, v);
+        epi_store_chunk<OUT_F32>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
+        sbuf ^= 1u;
+    }
+    const uint32_t row = (uint32_t)lane * 128u;
+    for (int c = oth0; c < oth1; ++c) {
+        uint32_t v[32];
+        epi_load_chunk<OUT_F32>(tmem_acc, lane_field, c, v);
+        const uint32_t slot = stage + (uint32_t)(c - oth0) * kEpiSlabBytes + row;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            st_shared_v4(slot + ((uint32_t)(j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();                       // staged partials visible to the TMA reduce
+    __syncwarp();
+    if (lane == 0) {
+        release();                                  // every accumulator column has been read
+        bulk_wait<0>();                             // own TMA stores complete
+        fence_proxy_async_all();
+    }
+    __syncwarp();
+    mbar_arrive_cluster(peer_bar);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(own_bar, 0, budget));
+    if (!ok) return false;
+    fence_proxy_async_all();                        // the peer's stores, acquired, before our reduces
+    if (lane == 0) {
+        for (int c = oth0; c < oth1; ++c) {
+            const int32_t nc = n0 + c * kChunkCols;
+            if (m0 < p.M && nc < p.n_tma)
+                tma_reduce_add_3d(tmC, stage + (uint32_t)(c - oth0) * kEpiSlabBytes, nc, m0, b);
+        }
+        bulk_commit();
+    }
+    const int32_t m = m0 + lane;
+    for (int c = oth0; c < oth1; ++c) {
+        const int32_t nc = n0 + c * kChunkCols;
+        if (nc + kChunkCols > p.n_tma && nc < p.N && m < p.M) {
+            // the ragged < 16-byte end of a row: not covered by the tensor map
+            float* rowp = static_cast<float*>(p.C) + (int64_t)b * p.strideC + (int64_t)m * p.ldc;
+            const uint32_t slot = stage + (uint32_t)(c - oth0) * kEpiSlabBytes + row;
+            const int32_t n_lo = max(p.n_tma, nc), n_hi = min(p.N, nc + kChunkCols);
+#pragma unroll 1
+            for (int32_t n = n_lo; n < n_hi; ++n) {
+                const uint32_t byte = (uint32_t)(n - nc) * 4u;
+                atomicAdd(rowp + n,
+                          __uint_as_float(ld_shared_u32(slot + ((((byte >> 4) ^ (uint32_t)(lane & 7)) << 4) |
+                                                                (byte & 15u)))));
+            }
+        }
+    }
+    return true;
+}
+
 // The last accumulator region of a tile with 16-bit output and 256 columns
 // (4 chunks): all four chunks are read from tensor memory into registers
 // first (128 per thread, packed), the accumulator is released, and only then

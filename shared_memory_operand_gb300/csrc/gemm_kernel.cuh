@@ -30,6 +30,16 @@
 // shared-memory load does in "A Deep Dive into LDS Optimizations on AMD
 // Instinct MI450 GPUs", Part I.
 //
+// Split-K (SPLIT = 1; fp32 output): the grid is one 2-CTA cluster per tile.
+// The CTA of cluster rank 0 computes the tile's first split_kh K blocks,
+// rank 1 the rest, each into its own tensor memory; the two partial sums
+// meet in global memory (see epilogue_split_tile): each CTA stores half of
+// the tile's columns plainly and adds its partial of the other half with TMA
+// reduce-adds once the peer's plain stores are complete.  A tile-starved
+// problem (fewer tiles than SMs) then runs on twice the SMs, each reading
+// half of the tile's K panel ("An Educational GEMM Ladder for Helios GPUs",
+// Level 3: large tiles leave a small problem with too few workgroups).
+//
 // Every mbarrier wait is bounded by p.timeout_ns of the global timer; on
 // timeout the thread records an error code, stops, and the CTA still drains
 // its in-flight copies and MMAs and frees tensor memory before returning.
@@ -43,15 +53,23 @@ namespace smo {
 
 static_assert(kStageKBytes / kMmaKBytes == 4, "the issue loops unroll four MMAs per K block");
 
-// KG: stages per full/empty barrier pair (1 or 2).  KIND: MmaKind.
-template <int OUT, int KG, int KIND>
+// KG: stages per full/empty barrier pair (1 or 2).  KIND: MmaKind.  SPLIT:
+// 1 = split-K over a 2-CTA cluster, one tile per cluster (fp32 output only).
+template <int OUT, int KG, int KIND, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+    static_assert(!SPLIT || OUT == OUT_F32, "split-K partials meet in fp32");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // tiles and K range of this CTA
+    const uint32_t crank = SPLIT ? (cluster_ctarank() & 1u) : 0u;
+    const int64_t tile0 = SPLIT ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    const int64_t tstride = SPLIT ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+    const int kb_begin = SPLIT && crank ? p.split_kh : 0;
+    const int kb_end = SPLIT && !crank ? p.split_kh : p.num_k;
 
     const uint32_t bars = base + p.off_bar;
     auto full_bar = [&](uint32_t s) { return bars + 8u * s; };
@@ -60,6 +78,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto acce_bar = [&](uint32_t b) { return bars + 8u * (2 * kMaxStages + 2 + b); };
     const uint32_t drain_bar = bars + 8u * (2 * kMaxStages + 4);
     const uint32_t tmem_slot = bars + 8u * (2 * kMaxStages + 5);
+    // SPLIT: every epilogue thread of the peer CTA arrives once its plain
+    // stores of the tile are complete
+    const uint32_t plain_bar = bars + 8u * (2 * kMaxStages + 6);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -71,6 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acce_bar(b), kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        if (SPLIT) mbar_init(plain_bar, kEpiWarps * 32);
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -84,7 +106,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (SPLIT) cluster_sync_all();      // the peer's barriers are initialised before any remote arrive
+    else __syncthreads();
     tc_fence_after();
     // The prologue above touches only shared memory, tensor memory and the
     // kernel parameters, so it may overlap the previous kernel in the stream
@@ -109,12 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t issued_mask = 0, issued_ph = 0;   // last issued phase per group (lane 0)
             bool skip_one = p.stall != 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            for (int64_t t = tile0; t < p.total_tiles && ok; t += tstride) {
                 int b, mb, nb;
                 decode_tile(p, t, b, mb, nb);
                 const int32_t mn0 = slot.is_a ? mb * kBM : nb * p.BN;
-                for (int kb = 0; kb < p.num_k; kb += KG) {
-                    const bool two = KG == 2 && kb + 1 < p.num_k;   // the last group may hold one block
+                for (int kb = kb_begin; kb < kb_end; kb += KG) {
+                    const bool two = KG == 2 && kb + 1 < kb_end;    // the last group may hold one block
                     int good = 1;
                     if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
                     good = __shfl_sync(lmask, good, 0);
@@ -178,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t so = 0;                           // group's descriptor offset
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
+            for (int64_t t = tile0; t < p.total_tiles && ok; t += tstride, ++it) {
                 const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
                 if (!mbar_wait(acce_bar(buf), aph ^ 1u, budget)) {
                     report_error(p.err, DEV_TIMEOUT_MMA);
@@ -187,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
-                for (int kb = 0; kb < p.num_k; kb += KG) {
+                for (int kb = kb_begin; kb < kb_end; kb += KG) {
                     if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
                         ok = false;
@@ -195,11 +218,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     uint64_t ad = a_desc0 + so, bd = b_desc0 + so;
-                    umma<KIND>(d_tmem, ad, bd, idesc, (uint32_t)(kb != 0));
+                    umma<KIND>(d_tmem, ad, bd, idesc, (uint32_t)(kb != kb_begin));
                     umma<KIND>(d_tmem, ad + ak, bd + bk, idesc, 1u);
                     umma<KIND>(d_tmem, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
                     umma<KIND>(d_tmem, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
-                    if (KG == 2 && kb + 1 < p.num_k) {
+                    if (KG == 2 && kb + 1 < kb_end) {
                         ad += stage_desc;
                         bd += stage_desc;
                         umma<KIND>(d_tmem, ad, bd, idesc, 1u);
@@ -229,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t q = (uint32_t)warp & 3u;           // TMEM lane quarter of this warp
         const uint32_t lane_field = (q * 32u) << 16;
         uint32_t it = 0, sbuf = 0;
-        for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+        for (int64_t t = tile0; t < p.total_tiles; t += tstride, ++it) {
             int b, mb, nb;
             decode_tile(p, t, b, mb, nb);
             const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
@@ -244,15 +267,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t m0 = mb * kBM + (int32_t)q * kEpiRowsPerWarp;
             const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
             const uint32_t acce = acce_bar(buf);
-            epilogue_tile<OUT>(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane, m0,
-                               nb * p.BN, b, [&] { mbar_arrive(acce); });
+            if constexpr (SPLIT) {
+                // one tile per cluster: the operand ring is idle once the
+                // accumulator is full; each warp stages the peer's chunks in
+                // its own 16 KiB of it
+                if (!epilogue_split_tile(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane,
+                                         m0, nb * p.BN, b, crank, base + q * 4u * kEpiSlabBytes,
+                                         mapa_shared(plain_bar, crank ^ 1u), plain_bar, budget,
+                                         [&] { mbar_arrive(acce); })) {
+                    if (lane == 0) report_error(p.err, DEV_TIMEOUT_SPLIT);
+                    break;
+                }
+            } else {
+                epilogue_tile<OUT>(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane, m0,
+                                   nb * p.BN, b, [&] { mbar_arrive(acce); });
+            }
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();
     }
 
     tc_fence_before();
-    __syncthreads();
+    if (SPLIT) cluster_sync_all();      // no CTA leaves while its peer may still arrive on its barrier
+    else __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }

@@ -39,6 +39,7 @@ enum DevErr : int32_t {
     DEV_TIMEOUT_EPILOGUE = 3,
     DEV_TIMEOUT_TEARDOWN = 4,
     DEV_TIMEOUT_FIXUP = 5,
+    DEV_TIMEOUT_SPLIT = 6,
 };
 
 struct KParams {
@@ -77,6 +78,10 @@ struct KParams {
     int64_t sk_units;
     float* sk_work;                 // one fp32 partial-accumulator slot per cluster
     int32_t* sk_flags;              // per stream-K tile: epilogue warps that published
+    // Split-K over a 2-CTA cluster (one-CTA kernel, fp32 output): the CTA of
+    // cluster rank 0 takes K blocks [0, split_kh), rank 1 [split_kh, num_k);
+    // 0 = no split.
+    int32_t split_kh;
     int32_t* err;                   // device error word
     int64_t timeout_ns;             // budget of each bounded wait
     int32_t stall;                  // test hook: skip the first TMA load

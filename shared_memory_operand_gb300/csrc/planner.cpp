@@ -162,7 +162,7 @@ uint32_t make_idesc(int in_dtype, int a_mn_major, int b_mn_major, int M, int N) 
 }
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
-               int out_dtype, int64_t batch, int num_sms, int force) {
+               int out_dtype, int64_t batch, int num_sms, int force, int split) {
     Plan p;
     p.M = M; p.N = N; p.K = K; p.batch = batch;
     p.in_dtype = in_dtype; p.out_dtype = out_dtype;
@@ -198,18 +198,72 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     const double cwide = (double)((twide + clusters - 1) / clusters) * 1.62;
     const bool long_k = p.num_k >= 48;
     int choice;
-    if (force == 128 || force == 256 || force == 512 || force == 1024) choice = force;
+    if (force == 128 || force == 192 || force == 256 || force == 384 || force == 512 || force == 1024) choice = force;
     else if (cpair <= c256 && cpair <= c128) choice = (long_k && cwide < cpair) ? 1024 : 512;
     else choice = (c128 < c256) ? 128 : 256;
-    p.pair = choice == 512 || choice == 1024;
+    // Split-K over a 2-CTA cluster (fp32 output): for a tile-starved problem
+    // -- one wave of one-CTA tiles on fewer SMs than the GPU has -- the two
+    // CTAs of each tile's cluster read half of its K panel each, on twice the
+    // SMs, and their partials meet in global memory.  Main-loop model,
+    // measured on GB300 with one-CTA tiles: an SM takes operands in at about
+    // 135 GB/s, and all SMs together at about 16 TB/s; the main loop lasts
+    // max(bytes per SM / 135 GB/s, total bytes / 16 TB/s).  The split's
+    // second pass over C (plain stores, their completion, then TMA
+    // reduce-adds) costs about 1.8 us more than one epilogue.  The split is
+    // taken for the tile width (128 / 192 / 256) whose two CTAs per tile fit
+    // one wave and whose modelled time beats the unsplit plan by more than
+    // that (measured: 512^2 x 4096 22.5 -> 15.4 us, 1024^2 x 1536 12.1 ->
+    // 10.9 us; 1500 x 1152 x 896 would lose 0.9 us and is not split).
+    const bool one_cta = choice == 128 || choice == 192 || choice == 256;
+    if (one_cta && out_dtype == 2 && p.num_k >= 2 && split != 0) {
+        auto main_us = [&](int64_t ctas, int bn, int64_t kblocks) {
+            const double per_cta = (double)(kBM + bn) * kSwizzleSpan * (double)kblocks;   // operand bytes
+            const int64_t waves = (ctas + p.num_sms - 1) / p.num_sms;
+            const int64_t active = std::min<int64_t>(ctas, p.num_sms);
+            const double per_sm_us = per_cta / 135e3;                                     // 135 GB/s
+            const double agg_us = per_cta * (double)active / 16e6;                          // 16 TB/s
+            return (double)waves * std::max(per_sm_us, agg_us);
+        };
+        const double base_us = main_us(tiles_for(kBM, choice), choice, p.num_k);
+        int sbn = 0;
+        double best = 0.0;
+        for (int bn : {128, 192, 256}) {
+            if (force == 128 || force == 192 || force == 256) {
+                if (bn != force) continue;
+            } else if (2 * tiles_for(kBM, bn) > p.num_sms) {
+                continue;
+            }
+            const double t = main_us(2 * tiles_for(kBM, bn), bn, (p.num_k + 1) / 2) + 1.8;
+            if (sbn == 0 || t < best) {
+                sbn = bn;
+                best = t;
+            }
+        }
+        const bool starved = tiles_for(kBM, choice) <= p.num_sms && sbn != 0 && best < base_us;
+        if (split == 1 || starved) {
+            p.split = 1;
+            choice = sbn != 0 ? sbn : 256;
+        }
+    }
+    p.pair = choice == 384 || choice == 512 || choice == 1024;
     p.wide = choice == 1024;
     p.tile_m = p.wide ? 4 * kBM : p.pair ? 2 * kBM : kBM;
-    const int bn = p.pair ? 256 : choice;
+    const int bn = choice == 384 ? 128 : p.pair ? 256 : choice;
     p.BN = bn;
     p.num_m = (int)((M + p.tile_m - 1) / p.tile_m);
     p.num_n = (int)((N + bn - 1) / bn);
     p.tiles = tiles_for(p.tile_m, bn);
-    p.grid = p.pair ? (int)(2 * std::min<int64_t>(p.tiles, clusters)) : (int)std::min<int64_t>(p.tiles, p.num_sms);
+    if (p.split) {
+        // one tile per cluster (the epilogue stages in the idle operand ring)
+        if (2 * p.tiles >= (1ll << 31)) {
+            p.why = "too many tiles for a split-K grid";
+            return p;
+        }
+        p.grid = (int)(2 * p.tiles);
+        p.split_kh = (p.num_k + 1) / 2;
+    } else {
+        p.grid = p.pair ? (int)(2 * std::min<int64_t>(p.tiles, clusters)) : (int)std::min<int64_t>(p.tiles, p.num_sms);
+    }
     p.group_m = std::min(p.pair ? 8 : 16, p.num_m);
     p.idesc = make_idesc(in_dtype, a_major, b_major, p.pair ? 2 * kBM : kBM, bn);
 
@@ -274,7 +328,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.off_epi = stages * p.stage_stride;
     p.off_bar = p.off_epi + epi_bytes;
     p.smem_bytes = p.off_bar + kBarrierBytes + 1024;
-    p.tmem_cols = 2 * bn;                          // two accumulators (power of two >= 32)
+    p.tmem_cols = 32;                              // two accumulators, allocated as a power of two >= 32
+    while (p.tmem_cols < (uint32_t)(2 * bn)) p.tmem_cols <<= 1;
+    // a split CTA stages its partial of the peer's half of the tile (4 warps x
+    // up to 4 chunks of 4 KiB) in the idle operand ring
+    if (p.split && (uint32_t)p.stages * p.stage_stride < kEpiWarps * 4 * kEpiSlabBytes) {
+        p.why = "operand ring too small to stage a split tile";
+        return p;
+    }
 
     bool layouts_ok = p.a.linear && p.a.bijective && p.a.tma_equals_umma && p.a.core_matrix_divides &&
                       p.b.linear && p.b.bijective && p.b.tma_equals_umma && p.b.core_matrix_divides &&
@@ -312,6 +373,7 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->tx_bytes = p.pair ? 2 * p.stage_stride : p.stage_stride;   // a pair's even CTA arms both CTAs' bytes
     kp->epi_chunk_cols = p.c.chunk_cols;
     kp->epi_chunks = p.c.chunks;
+    kp->split_kh = p.split ? p.split_kh : 0;
 }
 
 std::string describe_json(const Plan& p) {
@@ -333,7 +395,8 @@ std::string describe_json(const Plan& p) {
     };
     o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
       << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
-      << ",\"pair\":" << p.pair << ",\"wide\":" << p.wide << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
+      << ",\"pair\":" << p.pair << ",\"wide\":" << p.wide << ",\"split\":" << p.split
+      << ",\"split_kh\":" << p.split_kh << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
       << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads

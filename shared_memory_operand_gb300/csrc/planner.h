@@ -52,6 +52,8 @@ struct Plan {
     int kind = 0;                   // tcgen05.mma kind: 0 kind::f16, 1 kind::f8f6f4
     int pair = 0;                   // 1: CTA pair (cta_group::2), 256 x BN tiles over two SMs
     int wide = 0;                   // 1 (pair only): 512 x 256 tiles, 256 A rows per CTA, one accumulator
+    int split = 0;                  // 1 (one CTA, fp32 out): split-K over a 2-CTA cluster, one tile per cluster
+    int split_kh = 0;               // K blocks of the cluster's rank-0 CTA
     int tile_m = 128;               // output rows per tile (128; 256 for a pair; 512 for a wide pair)
     int BN = 256, stages = 4;
     int kgroup = 1;                 // stages per full/empty barrier pair
@@ -68,10 +70,13 @@ struct Plan {
 
 // in_dtype: 0 bf16, 1 f16, 3 FP8 E4M3, 4 FP8 E5M2.  out_dtype: 0 bf16, 1 f16,
 // 2 f32 (gemm_dtype_t).
-// force: 0 = choose; 128 or 256 = one CTA with that BN; 512 = CTA pair (256 x 256);
-// 1024 = wide CTA pair (512 x 256).
+// force: 0 = choose; 128, 192 or 256 = one CTA with that BN; 384 = CTA pair
+// with 256 x 128 tiles; 512 = CTA pair (256 x 256); 1024 = wide CTA pair
+// (512 x 256).
+// split: -1 = choose, 0 = never, 1 = split K over a 2-CTA cluster whenever the
+// plan allows it (one-CTA tiles, fp32 output, at least two K blocks).
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
-               int out_dtype, int64_t batch, int num_sms, int force);
+               int out_dtype, int64_t batch, int num_sms, int force, int split = -1);
 
 // Fills the kernel parameter block from a plan (pointers and runtime knobs are
 // set by the caller).

@@ -60,6 +60,30 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t
     }
 }
 
+// The same wait with acquire semantics at cluster scope: what the arriving
+// threads of another CTA of the cluster released before their arrive is
+// visible after it.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int64_t budget_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 15u) == 0 && (int64_t)(globaltimer() - t0) > budget_ns) return false;
+    }
+}
+
 // ---------------------------------------------------------------- fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -100,6 +124,18 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                      reinterpret_cast<uint64_t>(tmap)),
                  "r"(src), "r"(x), "r"(y), "r"(z)
                  : "memory");
+}
+
+// TMA reduce: adds a shared-memory tile into global memory element by
+// element (the tensor map's type: fp32 add, rounded to nearest), clipped to
+// the tensor's bounds like a store.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, uint32_t src, int32_t x, int32_t y,
+                                                  int32_t z) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
 }
 
 // Untiled bulk copy global -> this CTA's shared memory, completing `bytes` on

@@ -100,14 +100,17 @@ def test_planner_layouts_match_oracle(lib, am, bm, out):
         d = smo.gemm_plan_describe(M, N, K, am, bm, "bf16", out)
         assert d["ok"], d["why"]
         assert d["smem_bytes"] <= 232448
-        assert d["tmem_cols"] == 2 * d["BN"] and d["tmem_cols"] <= 512
+        # two accumulators, allocated as a power of two of columns
+        tc = d["tmem_cols"]
+        assert 2 * d["BN"] <= tc <= 512 and tc & (tc - 1) == 0 and tc < 4 * d["BN"]
         for name, major in (("A", am), ("B", bm)):
             op = d[name]
             tile = op["tile_mn"]          # per-CTA operand tile (half of BN in a pair)
             mn_major = bool(major)
             # planner's F2 basis images == oracle's 128B-swizzle TMA box layout
+            # (one basis per bit of the largest row index: 8 for 192 rows)
             want_mn = [banksim.operand_tile_offset(1 << i, 0, mn_major, tile)
-                       for i in range(tile.bit_length() - 1)]
+                       for i in range((tile - 1).bit_length())]
             want_k = [banksim.operand_tile_offset(0, 1 << i, mn_major, tile) for i in range(6)]
             assert op["basis_mn"] == want_mn
             assert op["basis_k"] == want_k
@@ -241,8 +244,25 @@ def test_instruction_descriptor_fp8_fields(lib):
 
 
 def test_tile_choice_and_grid(lib):
-    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
-    assert not d["pair"] and d["BN"] == 128 and d["tiles"] == 12 * 9 and d["grid"] == 108
+    # tile-starved: 128 x 128 one-CTA tiles on 108 SMs; splitting K (72 tiles of
+    # 128 x 192 on 144 SMs) is modelled, and measured, slower at K = 896
+    for out in ("f32", "f16"):
+        d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", out)
+        assert not d["pair"] and not d["split"] and d["BN"] == 128 and d["tiles"] == 12 * 9
+        assert d["grid"] == 108
+    # long K, few tiles, fp32 out: K split over 2-CTA clusters
+    d = smo.gemm_plan_describe(1500, 1152, 2688, 0, 1, "f16", "f32")
+    assert d["split"] and d["BN"] == 192 and d["tiles"] == 12 * 6 and d["grid"] == 144
+    assert d["split_kh"] == 21 and d["stages"] == 4 and d["tmem_cols"] == 512
+    x = d["idesc"]
+    assert ((x >> 24) & 31) * 16 == 128 and ((x >> 17) & 63) * 8 == 192
+    d = smo.gemm_plan_describe(512, 512, 4096, 0, 1, "bf16", "f32")
+    assert d["split"] and d["BN"] == 128 and d["grid"] == 32 and d["split_kh"] == 32
+    d = smo.gemm_plan_describe(512, 512, 4096, 0, 1, "bf16", "bf16")      # 16-bit out: never split
+    assert not d["split"] and d["grid"] == 16
+    # short K: no split
+    d = smo.gemm_plan_describe(256, 256, 256, 0, 1, "bf16", "f32")
+    assert not d["split"] and d["BN"] == 128 and d["grid"] == 4
     # long K: the wide pair (512 x 256 tiles); short K: 256 x 256
     d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
     assert d["pair"] and d["wide"] and d["BM"] == 512 and d["BN"] == 256 and d["tiles"] == 16 * 32
@@ -252,6 +272,32 @@ def test_tile_choice_and_grid(lib):
     assert d["grid"] == 152 and d["stages"] == 6 and d["A"]["tile_mn"] == d["B"]["tile_mn"] == 128
     d = smo.gemm_plan_describe(2048, 2048, 2048, 0, 1, "bf16", "bf16", batch=32)
     assert d["pair"] and d["tiles"] == 8 * 8 * 32
+
+
+def test_split_k_policy(lib, monkeypatch):
+    """Split-K is taken for fp32 output only, on one-CTA tiles; forced on it
+    still keeps at least one K block per CTA; forced off the plan is the
+    one-CTA 128 x 128 tiling."""
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "0")
+    d = smo.gemm_plan_describe(512, 512, 4096, 0, 1, "bf16", "f32")
+    assert not d["split"] and d["grid"] == 16
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "0")
+    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
+    assert not d["split"] and d["BN"] == 128 and d["grid"] == 108
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "1")
+    d = smo.gemm_plan_describe(256, 256, 256, 0, 1, "bf16", "f32")
+    assert d["split"] and d["split_kh"] == 2 and d["grid"] == 2 * d["tiles"]
+    d = smo.gemm_plan_describe(256, 256, 64, 0, 1, "bf16", "f32")       # one K block: nothing to split
+    assert not d["split"]
+    d = smo.gemm_plan_describe(256, 256, 256, 0, 1, "bf16", "bf16")      # 16-bit output: never split
+    assert not d["split"]
+    d = smo.gemm_plan_describe(4096, 4096, 4096, 0, 1, "bf16", "f32")    # CTA-pair plans: never split
+    assert d["pair"] and not d["split"]
+    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")      # forced on: narrowest one-wave width
+    assert d["split"] and d["BN"] == 192 and d["grid"] == 2 * 12 * 6 and d["split_kh"] == 7
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "256")
+    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
+    assert d["split"] and d["BN"] == 256 and d["grid"] == 2 * 12 * 5 and d["split_kh"] == 7
 
 
 def test_pair_descriptors(lib, monkeypatch):

@@ -43,7 +43,7 @@ def force_mode(monkeypatch):
 
 
 # ------------------------------------------------------------ every tile mode
-@pytest.mark.parametrize("mode", [128, 256, 512, 1024])
+@pytest.mark.parametrize("mode", [128, 192, 256, 512, 1024])
 @pytest.mark.parametrize("am,bm", MAJORS)
 def test_tile_modes_ragged(force_mode, mode, am, bm):
     force_mode(mode)
@@ -289,11 +289,19 @@ def test_config_256_bf16_f32():
     _full(workload("gemm_256_bf16_f32"))
 
 
-def test_config_1500x1152x896_f16_uniform():
+@pytest.mark.parametrize("split", ["auto", "0", "1"])
+def test_config_1500x1152x896_f16_uniform(split, monkeypatch):
+    """The planner splits K over 2-CTA clusters here (auto); forced off it runs
+    128 x 128 one-CTA tiles."""
+    if split != "auto":
+        monkeypatch.setenv("SMO_GEMM_SPLIT_K", split)
     _full(workload("gemm_1500x1152x896_f16_f32"))
 
 
-def test_config_1500x1152x896_f16_integer_bit_exact():
+@pytest.mark.parametrize("split", ["auto", "0", "1"])
+def test_config_1500x1152x896_f16_integer_bit_exact(split, monkeypatch):
+    if split != "auto":
+        monkeypatch.setenv("SMO_GEMM_SPLIT_K", split)
     _full(workload("gemm_1500x1152x896_f16_f32_int"), exact=True)
 
 
@@ -398,3 +406,62 @@ def test_stream_k_is_deterministic_and_matches_whole_tiles(monkeypatch):
     check(p, first, whole.astype(np.float64))               # same product, other split
     ref = oracle_full(p)
     check(p, first, ref)
+
+
+# ------------------------------------------------------------ split-K (one-CTA, 2-CTA clusters)
+@pytest.mark.parametrize("bn", ["", "128", "192", "256"])
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_split_k_full_compare(bn, am, bm, monkeypatch):
+    """K split over the two CTAs of a cluster; each output is the sum of the two
+    fp32 partials (one plain store, one TMA reduce-add).  Ragged M and N (the
+    reduce is clipped like a store; a ragged < 16-byte row end takes atomic
+    adds), K tails, odd K-block counts, a batch; integers bit-exact."""
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "1")
+    if bn:
+        monkeypatch.setenv("SMO_GEMM_FORCE_BN", bn)
+    for (M, N, K, batch, dist) in [(1500, 1152, 896, 1, "uniform"), (257, 513, 1000, 1, "uniform"),
+                                   (130, 261, 200, 2, "normal"), (384, 640, 960, 1, "int"),
+                                   (129, 258, 130, 1, "int"), (1, 4, 640, 1, "uniform")]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="bf16", out_dtype="f32", dist=dist,
+                         seed=M + N + K, batch=batch)
+        plan = smo.gemm_plan_describe(M, N, K, am, bm, "bf16", "f32", batch)
+        assert plan["split"] == 1
+        _full(p, exact=(dist == "int"))
+
+
+@pytest.mark.parametrize("M,N,K,dist", [(512, 512, 4096, "uniform"), (1500, 1152, 2688, "uniform"),
+                                        (1024, 1024, 2048, "int")])
+def test_split_k_chosen_by_planner(M, N, K, dist):
+    """Long K on few tiles with fp32 output: the planner splits K by itself."""
+    p = make_problem(M, N, K, a_major=K_MAJOR, b_major=MN_MAJOR, in_dtype="f16", out_dtype="f32", dist=dist,
+                     seed=K)
+    assert smo.gemm_plan_describe(M, N, K, K_MAJOR, MN_MAJOR, "f16", "f32")["split"] == 1
+    _full(p, exact=(dist == "int"))
+
+
+def test_split_k_is_deterministic(monkeypatch):
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "1")
+    p = workload("gemm_1500x1152x896_f16_f32")
+    first = run_gpu(p)
+    again = run_gpu(p)
+    assert np.array_equal(first, again)        # one rounding of two addends: order-free
+
+
+def test_split_k_timeout_reports_and_recovers(monkeypatch):
+    """A stalled stage in one CTA of a split cluster: its MMA wait, its
+    epilogue's wait and the peer's wait for its plain stores all run out; one
+    clean error, and the context stays usable."""
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "1")
+    old = smo.gemm_set_timeout_ns(20_000_000)
+    try:
+        smo.gemm_debug_inject_stall(True)
+        A = torch.zeros(1024, 1024, dtype=torch.bfloat16, device="cuda")
+        C = torch.zeros(1024, 1024, dtype=torch.float32, device="cuda")
+        smo.gemm_ex(A, 1024, 0, A, 1024, 1, C, 1024, 1024, 1024, 1024, out_dtype="f32")
+        assert smo.gemm_check() == smo.GEMM_ERR_TIMEOUT
+    finally:
+        smo.gemm_debug_inject_stall(False)
+        smo.gemm_set_timeout_ns(old)
+    assert smo.gemm_check() == smo.GEMM_OK
+    p = make_problem(1024, 1024, 1024, dist="uniform", seed=9, out_dtype="f32")
+    check(p, run_gpu(p), oracle_full(p))
