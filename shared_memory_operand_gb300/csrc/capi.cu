@@ -52,7 +52,7 @@ std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-using PlanKey = std::tuple<int64_t, int64_t, int64_t, int, int, int, int, int64_t, int, int, int>;
+using PlanKey = std::tuple<int64_t, int64_t, int64_t, int, int, int, int, int64_t, int, int, int, int>;
 std::map<PlanKey, Plan> g_plans;
 
 int elem_size(int dt) { return dt == GEMM_F32 ? 4 : (dt == GEMM_E4M3 || dt == GEMM_E5M2) ? 1 : 2; }
@@ -97,6 +97,15 @@ int force_bn_from_env() {
     if (!s) return 0;
     int v = std::atoi(s);
     return (v == 128 || v == 192 || v == 256 || v == 384 || v == 512 || v == 1024) ? v : 0;
+}
+
+// Measurement knob: tile width of wide CTA-pair tiles (a multiple of 16 up to
+// 256) instead of the planner's choice.
+int wide_bn_from_env() {
+    const char* s = std::getenv("SMO_GEMM_WIDE_BN");
+    if (!s) return 0;
+    const int v = std::atoi(s);
+    return (v >= 16 && v <= 256 && v % 16 == 0) ? v : 0;
 }
 
 // Split-K policy of the one-CTA kernel: SMO_GEMM_SPLIT_K=0 never, =1 whenever
@@ -162,12 +171,13 @@ Plan cached_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int 
                  int64_t batch, int num_sms) {
     int fbn = force_bn_from_env();
     int split = split_k_from_env();
-    PlanKey key{M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn, split};
+    int wbn = wide_bn_from_env();
+    PlanKey key{M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn, split, wbn};
     std::lock_guard<std::mutex> lk(g_mu);
     auto it = g_plans.find(key);
     if (it != g_plans.end()) return it->second;
     if (g_plans.size() > 4096) g_plans.clear();
-    Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn, split);
+    Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms, fbn, split, wbn);
     g_plans[key] = p;
     return p;
 }
@@ -530,12 +540,14 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     const int64_t b_outer = (b_major == GEMM_MN_MAJOR) ? K : N;
     CUtensorMap ta, tb, tc;
     // MN-major operands whose extent is a multiple of the 128-byte box width
-    // take one 4-D load per stage instead of one load per box.
+    // take one 4-D load per stage instead of one load per box -- when every
+    // CTA's operand tile starts on a box boundary (its width a multiple of
+    // the box width).
     const uint32_t aT = pl->a.box_inner, bT = pl->b.box_inner;
-    const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % aT == 0 &&
+    const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % aT == 0 && pl->a.tile_mn % aT == 0 &&
                          encode_fused(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox, aT,
                                       (uint32_t)pl->bk) == GEMM_OK;
-    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % bT == 0 &&
+    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % bT == 0 && pl->b.tile_mn % bT == 0 &&
                          encode_fused(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox, bT,
                                       (uint32_t)pl->bk) == GEMM_OK;
     if ((!a_fused &&
@@ -638,7 +650,7 @@ int64_t gemm_plan_describe(int64_t M, int64_t N, int64_t K, int a_major, int b_m
     int st = validate(M, N, K, a_major, b_major, in_dtype, out_dtype, batch);
     if (st != GEMM_OK) return st;
     Plan p = smo::make_plan(M, N, K, a_major, b_major, in_dtype, out_dtype, batch, num_sms > 0 ? num_sms : 1,
-                            force_bn_from_env(), split_k_from_env());
+                            force_bn_from_env(), split_k_from_env(), wide_bn_from_env());
     std::string s = smo::describe_json(p);
     if (buf && buflen > 0) {
         size_t n = s.size() < buflen - 1 ? s.size() : buflen - 1;

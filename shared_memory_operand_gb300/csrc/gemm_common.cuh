@@ -376,8 +376,49 @@ __device__ __forceinline__ void epi_store_chunk(const KParams& p, const CUtensor
     }
 }
 
+// A chunk of which only the first `cols` columns belong to the tile (the last
+// chunk of a tile whose width is not a whole number of 128-byte chunks): a
+// TMA store of the whole chunk would write into the next tile, so each lane
+// stores its own row's columns from registers, 16 bytes at a time (the
+// chunk starts 16-byte aligned: tile widths are multiples of 16 columns),
+// element by element past the matrix's last column N.
+template <int OUT>
+__device__ __forceinline__ void epi_store_partial(const KParams& p, int lane, int32_t m0, int32_t nc, int cols,
+                                                  int b, const uint32_t (&v)[32]) {
+    constexpr int kOutBytes = (OUT == OUT_F32) ? 4 : 2;
+    constexpr int kPer16 = 16 / kOutBytes;
+    const int32_t m = m0 + lane;
+    if (m >= p.M) return;
+    char* rowp = static_cast<char*>(p.C) + ((int64_t)b * p.strideC + (int64_t)m * p.ldc) * kOutBytes;
+    const int32_t n_hi = min(p.N, nc + cols);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int32_t n = nc + q * kPer16;
+        if (n + kPer16 <= n_hi) {
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(rowp + (int64_t)n * kOutBytes),
+                         "r"(v[4 * q]), "r"(v[4 * q + 1]), "r"(v[4 * q + 2]), "r"(v[4 * q + 3])
+                         : "memory");
+        } else if (n < n_hi) {
+            // static register indices only (a runtime index would move v to local memory)
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t word = v[4 * q + w];
+                if (OUT == OUT_F32) {
+                    const int32_t e = n + w;
+                    if (e < n_hi) *reinterpret_cast<uint32_t*>(rowp + (int64_t)e * 4) = word;
+                } else {
+                    const int32_t e = n + 2 * w;
+                    if (e < n_hi) *reinterpret_cast<uint16_t*>(rowp + (int64_t)e * 2) = (uint16_t)(word & 0xFFFFu);
+                    if (e + 1 < n_hi) *reinterpret_cast<uint16_t*>(rowp + (int64_t)(e + 1) * 2) = (uint16_t)(word >> 16);
+                }
+            }
+        }
+    }
+}
+
 // Epilogue of one accumulator tile for one warp: its 32 rows (TMEM lanes
-// 32*(warp % 4) ...), all p.epi_chunks column chunks of 128 bytes.
+// 32*(warp % 4) ...), all p.epi_chunks column chunks of 128 bytes (the last
+// one partial when the tile width is not a whole number of chunks).
 //   tmem_acc : tensor-memory address of the accumulator (lane field 0)
 //   slabs    : this warp's first staging slab (kEpiBufs slabs of kEpiSlabBytes)
 //   m0, n0   : first output row of the warp and first column of the tile
@@ -389,18 +430,26 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
                                               int32_t m0, int32_t n0, int b, Release release) {
     constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
     for (int c = 0; c < p.epi_chunks; ++c) {
+        const bool last = c == p.epi_chunks - 1;
+        const bool partial = last && p.epi_last_cols < kChunkCols;
         const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
-        if (lane == 0) bulk_wait_read<1>();        // this slab's previous store has read it
-        __syncwarp();
+        if (!partial) {
+            if (lane == 0) bulk_wait_read<1>();    // this slab's previous store has read it
+            __syncwarp();
+        }
         uint32_t v[32];
         epi_load_chunk<OUT>(tmem_acc, lane_field, c, v);
-        if (c == p.epi_chunks - 1) {
+        if (last) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) release();
         }
-        epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
-        sbuf ^= 1u;
+        if (partial) {
+            epi_store_partial<OUT>(p, lane, m0, n0 + c * kChunkCols, p.epi_last_cols, b, v);
+        } else {
+            epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
+            sbuf ^= 1u;
+        }
     }
 }
 

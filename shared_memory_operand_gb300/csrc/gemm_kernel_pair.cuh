@@ -341,9 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
                                    (int32_t)q * kEpiRowsPerWarp;
                 if constexpr (WIDE && OUT != OUT_F32) {
-                    if (i == MSUB - 1) {
+                    if (i == MSUB - 1 && p.BN == 256) {
                         // the single accumulator: hand it back to the MMA issuer
-                        // as soon as the last region sits in registers
+                        // as soon as the last region sits in registers (four
+                        // whole 64-column chunks; a narrower wide tile takes
+                        // the chunk-by-chunk path below)
                         epilogue_region_early_release<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
                                                            sbuf, lane, m0, nb * p.BN, b,
                                                            [&] { mbar_arrive_cluster(acce); });

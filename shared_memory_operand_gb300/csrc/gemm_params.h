@@ -65,7 +65,8 @@ struct KParams {
     uint32_t tmem_cols;
     uint32_t tx_bytes;              // bytes TMA delivers per stage
     int32_t epi_chunk_cols;         // output columns per 128-byte chunk
-    int32_t epi_chunks;             // chunks per tile row (BN / epi_chunk_cols)
+    int32_t epi_chunks;             // chunks per tile row (ceil(BN / epi_chunk_cols))
+    int32_t epi_last_cols;          // tile columns in the last chunk (epi_chunk_cols unless BN is not a multiple)
     void* C;                        // output base (ragged 16-byte row tails are stored directly)
     int64_t ldc, strideC;           // elements
     int32_t n_tma;                  // columns [0, n_tma) are written by TMA (n_tma * es % 16 == 0)

@@ -83,7 +83,7 @@ void plan_operand(OperandPlan& op, int mn_major, int tile_mn, int es) {
     } else {
         op.box_inner = T;                // MN, 128 bytes
         op.box_outer = op.bk;            // K rows
-        op.nbox = tile_mn / (int)T;
+        op.nbox = (tile_mn + (int)T - 1) / (int)T;   // the last box may reach past the tile
         op.box_bytes = op.bk * kSwizzleSpan;
         op.lbo = op.box_bytes;           // next 128-byte-wide MN atom = next box
         op.sbo = kSwizzleAtom;           // next group of 8 k rows
@@ -93,21 +93,27 @@ void plan_operand(OperandPlan& op, int mn_major, int tile_mn, int es) {
     op.desc_hi = desc_hi(op.lbo, op.sbo);
 
     // ---- F2 model and checks ------------------------------------------------
-    op.bits_mn = log2i(tile_mn);
+    // The stage holds what TMA writes: tile_mn rows of a K-major operand, or
+    // nbox whole 128-byte-wide boxes of an MN-major one (loaded_mn >= tile_mn
+    // when the tile is not a whole number of boxes; the MMA reads the first
+    // tile_mn).  Linearity and bijectivity are checked over what is loaded,
+    // TMA == tensor core over what the MMA reads.
+    const uint32_t loaded_mn = op.mn_major ? (uint32_t)op.nbox * T : (uint32_t)tile_mn;
+    op.bits_mn = log2i(loaded_mn);
     op.bits_k = log2i(op.bk);
     for (int i = 0; i < op.bits_mn; ++i) op.basis_mn[i] = tma_offset(op, 1u << i, 0);
     for (int i = 0; i < op.bits_k; ++i) op.basis_k[i] = tma_offset(op, 0, 1u << i);
     bool linear = true, same = true;
     std::vector<uint8_t> hit(op.nbox > 0 ? op.stage_bytes / es : 0, 0);
     bool inj = op.nbox > 0;
-    for (uint32_t mn = 0; mn < (uint32_t)tile_mn; ++mn) {
+    for (uint32_t mn = 0; mn < loaded_mn; ++mn) {
         for (uint32_t k = 0; k < (uint32_t)op.bk; ++k) {
             uint32_t t = tma_offset(op, mn, k);
             uint32_t x = 0;
             for (int i = 0; i < op.bits_mn; ++i) if ((mn >> i) & 1) x ^= op.basis_mn[i];
             for (int i = 0; i < op.bits_k; ++i) if ((k >> i) & 1) x ^= op.basis_k[i];
             linear &= (x == t);
-            same &= (umma_offset(op, mn, k) == t);
+            if (mn < (uint32_t)tile_mn) same &= (umma_offset(op, mn, k) == t);
             if (t / es >= hit.size() || hit[t / es]) inj = false; else hit[t / es] = 1;
         }
     }
@@ -162,7 +168,7 @@ uint32_t make_idesc(int in_dtype, int a_mn_major, int b_mn_major, int M, int N) 
 }
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
-               int out_dtype, int64_t batch, int num_sms, int force, int split) {
+               int out_dtype, int64_t batch, int num_sms, int force, int split, int wide_bn) {
     Plan p;
     p.M = M; p.N = N; p.K = K; p.batch = batch;
     p.in_dtype = in_dtype; p.out_dtype = out_dtype;
@@ -248,7 +254,30 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.pair = choice == 384 || choice == 512 || choice == 1024;
     p.wide = choice == 1024;
     p.tile_m = p.wide ? 4 * kBM : p.pair ? 2 * kBM : kBM;
-    const int bn = choice == 384 ? 128 : p.pair ? 256 : choice;
+    int bn = choice == 384 ? 128 : p.pair ? 256 : choice;
+    if (p.wide) {
+        // Wave quantisation of wide tiles: a narrower tile (still a multiple
+        // of 16 columns, so that each CTA's half is a whole number of 8-column
+        // core matrices) takes proportionally fewer tensor cycles, so a width
+        // whose tile count fills the last wave better can win: 4096^2 has 128
+        // tiles of 512 x 256 on 76 clusters (1.68 waves, run as 2), but 152 of
+        // 512 x 224 (exactly 2 waves of 7/8 the work each).  Ties keep 256.
+        if (wide_bn >= 16 && wide_bn <= 256 && wide_bn % 16 == 0) {
+            bn = wide_bn;
+        } else {
+            double best = 0.0;
+            for (int w : {256, 240, 224, 208, 192}) {
+                // an N-major B half-tile must start on a 16-byte boundary (TMA)
+                if (b_major && ((w / 2) * p.in_es) % 16 != 0) continue;
+                const int64_t t = tiles_for(4 * kBM, w);
+                const double cost = (double)((t + clusters - 1) / clusters) * (double)w / 256.0;
+                if (w == 256 || cost < best - 1e-9) {
+                    best = cost;
+                    bn = w;
+                }
+            }
+        }
+    }
     p.BN = bn;
     p.num_m = (int)((M + p.tile_m - 1) / p.tile_m);
     p.num_n = (int)((N + bn - 1) / bn);
@@ -272,9 +301,27 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     plan_operand(p.a, a_major, p.wide ? 2 * kBM : kBM, p.in_es);
     plan_operand(p.b, b_major, p.pair ? bn / 2 : bn, p.in_es);
 
+    // TMA rule: a tiled copy's innermost coordinate times the element size
+    // must be a multiple of 16 bytes, or the copy faults.  For an MN-major
+    // operand that coordinate is the tile's MN origin (a multiple of the tile
+    // step) plus the CTA's offset inside a pair tile (a multiple of its own
+    // tile) plus whole 128-byte boxes; for a K-major operand it is a multiple
+    // of the 128-byte stage.  The C map's innermost coordinate is a tile's
+    // column origin plus whole 128-byte chunks.  A plan that breaks this is
+    // never launched.
+    auto x_aligned = [](int64_t elems, int es) { return (elems * es) % 16 == 0; };
+    const bool a_ok = !a_major || (x_aligned(p.tile_m, p.in_es) && x_aligned(p.a.tile_mn, p.in_es));
+    const bool b_ok = !b_major || (x_aligned(bn, p.in_es) && x_aligned(p.b.tile_mn, p.in_es));
+    const bool c_ok = x_aligned(bn, out_dtype == 2 ? 4 : 2);
+    if (!a_ok || !b_ok || !c_ok) {
+        p.why = "tile width breaks the 16-byte TMA coordinate rule";
+        return p;
+    }
+
     p.c.out_es = (out_dtype == 2) ? 4 : 2;
     p.c.chunk_cols = 128 / p.c.out_es;
-    p.c.chunks = bn / p.c.chunk_cols;
+    p.c.chunks = (bn + p.c.chunk_cols - 1) / p.c.chunk_cols;
+    p.c.last_cols = bn - (p.c.chunks - 1) * p.c.chunk_cols;
     for (int i = 0; i < 5; ++i) p.c.basis_row[i] = epi_offset(1u << i, 0);
     for (int i = 0; i < 3; ++i) p.c.basis_chunk[i] = epi_offset(0, 1u << i);
     {
@@ -373,6 +420,7 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->tx_bytes = p.pair ? 2 * p.stage_stride : p.stage_stride;   // a pair's even CTA arms both CTAs' bytes
     kp->epi_chunk_cols = p.c.chunk_cols;
     kp->epi_chunks = p.c.chunks;
+    kp->epi_last_cols = p.c.last_cols;
     kp->split_kh = p.split ? p.split_kh : 0;
 }
 
@@ -408,7 +456,7 @@ std::string describe_json(const Plan& p) {
     o << ",\"B\":";
     op_json(p.b);
     o << ",\"C\":{\"out_es\":" << p.c.out_es << ",\"chunk_cols\":" << p.c.chunk_cols
-      << ",\"chunks\":" << p.c.chunks << ",\"slab_bytes\":" << kEpiSlabBytes
+      << ",\"chunks\":" << p.c.chunks << ",\"last_cols\":" << p.c.last_cols << ",\"slab_bytes\":" << kEpiSlabBytes
       << ",\"bufs\":" << kEpiBufs << ",\"basis_row\":[";
     for (int i = 0; i < 5; ++i) o << (i ? "," : "") << p.c.basis_row[i];
     o << "],\"basis_chunk\":[";

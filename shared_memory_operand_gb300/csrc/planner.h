@@ -38,7 +38,8 @@ struct OperandPlan {
 struct EpiPlan {
     int out_es = 4;
     int chunk_cols = 32;
-    int chunks = 0;
+    int chunks = 0;                 // ceil(BN / chunk_cols)
+    int last_cols = 32;             // tile columns in the last chunk
     uint32_t basis_row[5] = {0}, basis_chunk[3] = {0};
     bool bijective = false;
     int planner_degree = 0;         // planner's own bank-degree estimate of one store
@@ -75,8 +76,10 @@ struct Plan {
 // (512 x 256).
 // split: -1 = choose, 0 = never, 1 = split K over a 2-CTA cluster whenever the
 // plan allows it (one-CTA tiles, fp32 output, at least two K blocks).
+// wide_bn: tile width of a wide CTA pair (0 = choose among 256, 240, 224, 208,
+// 192 by wave quantisation; otherwise that width, a multiple of 16 <= 256).
 Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in_dtype,
-               int out_dtype, int64_t batch, int num_sms, int force, int split = -1);
+               int out_dtype, int64_t batch, int num_sms, int force, int split = -1, int wide_bn = 0);
 
 // Fills the kernel parameter block from a plan (pointers and runtime knobs are
 // set by the caller).

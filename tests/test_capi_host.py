@@ -123,7 +123,10 @@ def test_planner_layouts_match_oracle(lib, am, bm, out):
                         banksim.operand_tile_offset(mn, k, mn_major, tile)
             assert op["linear"] and op["bijective"] and op["tma_equals_umma"]
             assert op["core_matrix_divides"]
-            assert op["stage_bytes"] == tile * 64 * 2
+            # K-major: tile rows of 128 bytes; MN-major: whole 64-wide boxes
+            # (a tile of 112 columns loads two, the MMA reads the first 112)
+            loaded = -(-tile // 64) * 64 if mn_major else tile
+            assert op["stage_bytes"] == loaded * 64 * 2
 
 
 @pytest.mark.parametrize("am", [0, 1])
@@ -142,8 +145,9 @@ def test_planner_fp8_layouts_match_oracle(lib, am, bm, ind):
             op = d[name]
             tile = op["tile_mn"]
             mn_major = bool(major)
+            loaded = -(-tile // 128) * 128 if mn_major else tile
             want_mn = [banksim.operand_tile_offset(1 << i, 0, mn_major, tile, elem_bytes=1, box_k=128)
-                       for i in range(tile.bit_length() - 1)]
+                       for i in range((loaded - 1).bit_length())]
             want_k = [banksim.operand_tile_offset(0, 1 << i, mn_major, tile, elem_bytes=1, box_k=128)
                       for i in range(7)]
             assert op["basis_mn"] == want_mn
@@ -155,7 +159,7 @@ def test_planner_fp8_layouts_match_oracle(lib, am, bm, ind):
                         banksim.operand_tile_offset(mn, k, mn_major, tile, elem_bytes=1, box_k=128)
             assert op["linear"] and op["bijective"] and op["tma_equals_umma"]
             assert op["core_matrix_divides"]
-            assert op["stage_bytes"] == tile * 128
+            assert op["stage_bytes"] == loaded * 128
             assert op["box"] == ([128, tile] if not mn_major else [128, 128])
 
 
@@ -167,6 +171,7 @@ def test_wide_pair_plans(lib, monkeypatch, am, bm, ind):
     second 128-row half starts 16 KiB into the stage in every layout (the
     offset the issue loop adds); 4 stages of 48 KiB, one per barrier pair."""
     monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    monkeypatch.setenv("SMO_GEMM_WIDE_BN", "256")
     es = 1 if ind == "e4m3" else 2
     bk = 128 // es
     for (M, N, K) in [(8192, 8192, 8192), (1500, 1152, 896), (129, 257, 65)]:
@@ -298,6 +303,58 @@ def test_split_k_policy(lib, monkeypatch):
     monkeypatch.setenv("SMO_GEMM_FORCE_BN", "256")
     d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")
     assert d["split"] and d["BN"] == 256 and d["grid"] == 2 * 12 * 5 and d["split_kh"] == 7
+
+
+def test_wide_tile_width_by_wave_quantisation(lib):
+    """4096^2 on 76 clusters: 128 tiles of 512 x 256 run in 2 waves, the
+    second 52/76 full; 152 tiles of 512 x 224 fill both waves exactly with 7/8
+    of the work per tile.  8192^2: 512 x 256 tiles (7 waves), as 224 would
+    need 8.  Each CTA then stages 112 B columns: one 112-row box (K-major) or
+    two 64-wide boxes (N-major, the MMA reading the first 112); the bf16
+    epilogue has 3 whole 64-column chunks and a 32-column one."""
+    for am in (0, 1):
+        for bm in (0, 1):
+            d = smo.gemm_plan_describe(4096, 4096, 4096, am, bm, "bf16", "bf16")
+            assert d["wide"] and d["BN"] == 224 and d["tiles"] == 8 * 19 and d["grid"] == 152
+            B = d["B"]
+            assert B["tile_mn"] == 112
+            assert (B["nbox"], B["stage_bytes"]) == ((2, 16384) if bm else (1, 112 * 128))
+            assert B["linear"] and B["bijective"] and B["tma_equals_umma"] and B["core_matrix_divides"]
+            assert d["C"]["chunks"] == 4 and d["C"]["last_cols"] == 32
+            x = d["idesc"]
+            assert ((x >> 24) & 31) * 16 == 256 and ((x >> 17) & 63) * 8 == 224
+            assert d["tmem_cols"] == 512
+    d = smo.gemm_plan_describe(4096, 4096, 4096, 0, 1, "bf16", "f32")
+    assert d["BN"] == 224 and d["C"]["chunks"] == 7 and d["C"]["last_cols"] == 32
+    d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
+    assert d["wide"] and d["BN"] == 256 and d["C"]["chunks"] == 4 and d["C"]["last_cols"] == 64
+
+
+def test_tma_coordinate_rule_refuses_unaligned_widths(lib, monkeypatch):
+    """A tiled TMA copy whose innermost coordinate times the element size is
+    not a multiple of 16 bytes faults the GPU.  With one-byte operands and an
+    N-major B, a pair tile of width w gives each CTA w / 2 columns: w / 2 must
+    be a multiple of 16.  The planner refuses such a forced width (no launch)
+    and its own choice never takes one."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    for w in (208, 240, 112, 48):
+        monkeypatch.setenv("SMO_GEMM_WIDE_BN", str(w))
+        d = smo.gemm_plan_describe(600, 700, 384, 0, 1, "e4m3", "bf16")
+        assert not d["ok"] and "TMA" in d["why"]
+        assert smo.gemm_plan_describe(600, 700, 384, 0, 0, "e4m3", "bf16")["ok"]     # K-major B: fine
+        assert smo.gemm_plan_describe(600, 700, 384, 0, 1, "bf16", "bf16")["ok"]     # 2-byte: fine
+    monkeypatch.delenv("SMO_GEMM_WIDE_BN")
+    for M, N in [(4096, 4096), (2048, 6144), (1536, 1000)]:
+        d = smo.gemm_plan_describe(M, N, 8192, 0, 1, "e4m3", "bf16")
+        assert d["ok"] and (d["BN"] // 2) % 16 == 0
+    # every plan's MN-major coordinates are 16-byte aligned, whatever the width
+    for w in range(16, 257, 16):
+        monkeypatch.setenv("SMO_GEMM_WIDE_BN", str(w))
+        for ind, es in (("bf16", 2), ("e4m3", 1)):
+            d = smo.gemm_plan_describe(1000, 1000, 512, 1, 1, ind, "bf16")
+            if d["ok"]:
+                assert (d["BN"] * es) % 16 == 0 and (d["B"]["tile_mn"] * es) % 16 == 0
+                assert (d["A"]["tile_mn"] * es) % 16 == 0
 
 
 def test_pair_descriptors(lib, monkeypatch):

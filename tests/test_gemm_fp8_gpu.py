@@ -119,3 +119,30 @@ def test_config_8192_fp8(name):
 
 def test_config_8192_fp8_integer_bit_exact():
     _full(workload("gemm_8192_e4m3_bf16_AK_BN", dist="int", out_dtype="f32"), exact=True)
+
+
+@pytest.mark.parametrize("wbn", [224, 192, 160])
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_wide_tile_widths_fp8(wbn, am, bm, monkeypatch):
+    """FP8 operands on 512 x wbn CTA-pair tiles (an N-major box is 128 values
+    wide, so every half-width here is one box; each half starts on a 16-byte
+    boundary, as TMA requires -- widths whose half does not are refused by the
+    planner, tests/test_capi_host.py)."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    monkeypatch.setenv("SMO_GEMM_WIDE_BN", str(wbn))
+    for (M, N, K, out, dist) in [(600, 700, 384, "bf16", "uniform"), (1100, 1030, 520, "f32", "int")]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="e4m3", out_dtype=out, dist=dist,
+                         seed=M + wbn)
+        _full(p, exact=(dist == "int"))
+
+
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_split_k_fp8(am, bm, monkeypatch):
+    """Split-K over 2-CTA clusters with FP8 operands (fp32 output): 192-wide
+    tiles, whose N-major B takes two 128-wide FP8 boxes per stage."""
+    monkeypatch.setenv("SMO_GEMM_SPLIT_K", "1")
+    for (M, N, K, dist) in [(1500, 1152, 896, "uniform"), (600, 700, 1000, "int")]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype="e4m3", out_dtype="f32", dist=dist,
+                         seed=M + K)
+        assert smo.gemm_plan_describe(M, N, K, am, bm, "e4m3", "f32")["split"] == 1
+        _full(p, exact=(dist == "int"))

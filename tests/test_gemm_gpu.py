@@ -465,3 +465,26 @@ def test_split_k_timeout_reports_and_recovers(monkeypatch):
     assert smo.gemm_check() == smo.GEMM_OK
     p = make_problem(1024, 1024, 1024, dist="uniform", seed=9, out_dtype="f32")
     check(p, run_gpu(p), oracle_full(p))
+
+
+# ------------------------------------------------------------ wide tiles narrower than 256
+@pytest.mark.parametrize("wbn", [256, 240, 224, 208, 192, 112, 48, 16])
+@pytest.mark.parametrize("am,bm", MAJORS)
+def test_wide_tile_widths(wbn, am, bm, monkeypatch):
+    """512 x wbn CTA-pair tiles: each CTA stages wbn / 2 B columns (a K-major
+    box of that many rows, or whole 64-wide N-major boxes of which the MMA
+    reads the first wbn / 2), and the epilogue's last chunk may be partial
+    (stored directly, never into the next tile).  Ragged edges, a batch,
+    three output types; integers bit-exact."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    monkeypatch.setenv("SMO_GEMM_WIDE_BN", str(wbn))
+    for (M, N, K, ind, out, dist, batch) in [(600, 700, 300, "bf16", "bf16", "uniform", 1),
+                                              (1100, 1030, 520, "bf16", "f32", "normal", 1),
+                                              (520, 1000, 1000, "f16", "f16", "uniform", 1),
+                                              (257, 513, 129, "bf16", "f32", "int", 2),
+                                              (1024, 896, 256, "bf16", "bf16", "int", 1)]:
+        p = make_problem(M, N, K, a_major=am, b_major=bm, in_dtype=ind, out_dtype=out, dist=dist,
+                         seed=M + N + wbn, batch=batch)
+        plan = smo.gemm_plan_describe(M, N, K, am, bm, ind, out, batch)
+        assert plan["wide"] == 1 and plan["BN"] == wbn
+        _full(p, exact=(dist == "int"))
