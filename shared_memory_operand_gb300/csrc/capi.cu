@@ -35,8 +35,8 @@ struct DevState {
     int32_t* d_err = nullptr;
     bool attr_set[12] = {};         // one-CTA kernels: [(KIND * 3 + OUT) * 2 + KG - 1]
     bool split_attr_set[4] = {};    // split-K one-CTA kernels (fp32 out): [KIND * 2 + KG - 1]
-    bool pair_attr_set[12] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT]
-    int pair_max_clusters[12] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
+    bool pair_attr_set[18] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT], WIDE 0..2
+    int pair_max_clusters[18] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
     // Stream-K workspace, one per stream so that GEMMs running concurrently
     // on different streams never share partial slots or tile counters.
     struct SkWork {
@@ -413,8 +413,13 @@ template <int OUT, int KIND>
 int launch_kind(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KParams& kp, cudaStream_t stream, int stream_k) {
     if (!pl.pair) return launch_single<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream);
-    return pl.wide ? launch_pair<OUT, KIND, 1>(pl, ds, ta, tb, tc, kp, stream, stream_k)
-                   : launch_pair<OUT, KIND, 0>(pl, ds, ta, tb, tc, kp, stream, stream_k);
+    if (!pl.wide) return launch_pair<OUT, KIND, 0>(pl, ds, ta, tb, tc, kp, stream, stream_k);
+    if constexpr (OUT != smo::OUT_F32) {
+        // 193 .. 255 columns: the variant with a partial last chunk
+        if (pl.c.chunks == 4 && pl.c.last_cols < 64)
+            return launch_pair<OUT, KIND, 2>(pl, ds, ta, tb, tc, kp, stream, stream_k);
+    }
+    return launch_pair<OUT, KIND, 1>(pl, ds, ta, tb, tc, kp, stream, stream_k);
 }
 
 template <int OUT>

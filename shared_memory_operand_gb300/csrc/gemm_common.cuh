@@ -544,7 +544,9 @@ __device__ __forceinline__ bool epilogue_split_tile(const KParams& p, const CUte
 // first (128 per thread, packed), the accumulator is released, and only then
 // are the chunks staged and stored -- the MMA issuer waits for four tensor
 // memory reads instead of four whole chunk round trips.
-template <int OUT, typename Release>
+// PARTIAL = 1: a tile of 193 .. 255 columns (4 chunks, the last one holding
+// p.epi_last_cols < 64 of them), whose last chunk is stored directly.
+template <int OUT, int PARTIAL, typename Release>
 __device__ __forceinline__ void epilogue_region_early_release(const KParams& p, const CUtensorMap* tmC,
                                                               uint32_t tmem_acc, uint32_t lane_field,
                                                               uint32_t slabs, uint32_t& sbuf, int lane, int32_t m0,
@@ -559,13 +561,15 @@ __device__ __forceinline__ void epilogue_region_early_release(const KParams& p, 
     __syncwarp();
     if (lane == 0) release();
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
+    for (int c = 0; c < kChunks - PARTIAL; ++c) {
         const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
         if (lane == 0) bulk_wait_read<1>();
         __syncwarp();
         epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * 64, b, v[c]);
         sbuf ^= 1u;
     }
+    if constexpr (PARTIAL)
+        epi_store_partial<OUT>(p, lane, m0, n0 + (kChunks - 1) * 64, p.epi_last_cols, b, v[kChunks - 1]);
 }
 
 }  // namespace smo

@@ -43,6 +43,10 @@ constexpr uint32_t kHalfABytes = kBM * kStageKBytes;   // 128 A rows of one stag
 // KIND: MmaKind (kind::f16 for 16-bit operands, kind::f8f6f4 for FP8).
 // WIDE: 0 -- 256 x 256 tiles, 128 A rows per CTA, two accumulators, stages
 //            handed over in groups of two (6 x 32 KiB);
+//       2 -- as 1, for tiles 193 .. 255 columns wide with 16-bit output: the
+//            last 64-column chunk is partial and stored directly, still after
+//            the early hand-back of the accumulator (a variant of its own, so
+//            that the 256-wide kernel keeps its registers);
 //       1 -- 512 x 256 tiles, 256 A rows per CTA (two 128-row halves, each
 //            with its own 256 x 256 MMAs into TMEM columns 0..255 / 256..511),
 //            one accumulator, one stage per barrier pair (4 x 48 KiB).  The B
@@ -53,6 +57,7 @@ template <int OUT, int KIND, int WIDE>
 __global__ void __launch_bounds__(kThreads, 1)
     smo_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
+    static_assert(WIDE != 2 || OUT != OUT_F32, "partial-chunk variant: 16-bit output");
     constexpr int KG = WIDE ? 1 : kPairGroup;      // stages per full/empty barrier pair
     constexpr int MSUB = WIDE ? 2 : 1;             // 128-row A halves (and accumulator regions) per CTA
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -341,12 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
                                    (int32_t)q * kEpiRowsPerWarp;
                 if constexpr (WIDE && OUT != OUT_F32) {
-                    if (i == MSUB - 1 && p.BN == 256) {
+                    if (i == MSUB - 1 && (WIDE == 2 || p.BN == 256)) {
                         // the single accumulator: hand it back to the MMA issuer
                         // as soon as the last region sits in registers (four
                         // whole 64-column chunks; a narrower wide tile takes
                         // the chunk-by-chunk path below)
-                        epilogue_region_early_release<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
+                        epilogue_region_early_release<OUT, WIDE == 2>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
                                                            sbuf, lane, m0, nb * p.BN, b,
                                                            [&] { mbar_arrive_cluster(acce); });
                         continue;

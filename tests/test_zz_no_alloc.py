@@ -14,9 +14,9 @@ depends on the allocating entry points having run first.
 Checked here:
   * two calls in a row give the output of the existing entry point gemm_ex,
     and the oracle's, within the parity tests' tolerances, on problems that
-    run each kernel: one CTA (BN = 128 and 256), the CTA pair with 256 x 256
-    tiles and with 512 x 256 tiles, fp32 and 16-bit output, both B
-    orientations, a ragged shape and a batch;
+    run each kernel: one CTA (BN = 128), split K over a 2-CTA cluster, the
+    CTA pair with 256 x 256 tiles and with 512 x 256 and 512 x 224 tiles, fp32
+    and 16-bit output, both B orientations, a ragged shape and a batch;
   * a bounded-wait timeout of this variant is reported by gemm_check_noalloc,
     survives a later call until it is reported, is cleared by the report, and
     the next call is correct;
@@ -50,9 +50,15 @@ PROBLEMS = {
     "one_cta_batch": lambda: make_problem(256, 384, 192, batch=3, out_dtype="bf16", dist="uniform", seed=7),
     "pair_256x256": lambda: make_problem(2048, 2048, 256, in_dtype="bf16", out_dtype="bf16",
                                          dist="uniform", seed=8),
-    "pair_512x256": lambda: make_problem(2560, 3072, 3072, a_major=K_MAJOR, b_major=MN_MAJOR,
+    "pair_512x256": lambda: make_problem(3072, 3072, 3072, a_major=K_MAJOR, b_major=MN_MAJOR,
                                          in_dtype="bf16", out_dtype="bf16", dist="uniform", seed=9),
+    "pair_512x224": lambda: make_problem(2048, 4096, 3072, a_major=K_MAJOR, b_major=MN_MAJOR,
+                                         in_dtype="bf16", out_dtype="bf16", dist="uniform", seed=10),
+    "split_k": lambda: make_problem(512, 512, 4096, a_major=K_MAJOR, b_major=MN_MAJOR,
+                                    in_dtype="bf16", out_dtype="f32", dist="uniform", seed=11),
 }
+# tile width the planner picks (wide pairs) / whether it splits K
+WIDTH = {"pair_512x256": 256, "pair_512x224": 224}
 
 
 def _noalloc(p):
@@ -62,10 +68,13 @@ def _noalloc(p):
 @pytest.mark.parametrize("name", list(PROBLEMS))
 def test_noalloc_matches_gemm_ex_and_oracle_twice(name):
     p = PROBLEMS[name]()
+    plan = smo.gemm_plan_describe(p.M, p.N, p.K, p.a_major, p.b_major, p.in_dtype, p.out_dtype,
+                                  p.batch, torch.cuda.get_device_properties(0).multi_processor_count)
     if name.startswith("pair"):
-        plan = smo.gemm_plan_describe(p.M, p.N, p.K, p.a_major, p.b_major, p.in_dtype, p.out_dtype,
-                                      p.batch, torch.cuda.get_device_properties(0).multi_processor_count)
-        assert plan["pair"] == 1 and plan["wide"] == (1 if name == "pair_512x256" else 0)
+        assert plan["pair"] == 1 and plan["wide"] == (1 if name in WIDTH else 0)
+        if name in WIDTH:
+            assert plan["BN"] == WIDTH[name]
+    assert plan["split"] == (1 if name == "split_k" else 0)
     ref = oracle_full(p)
     existing = run_gpu(p)                              # the allocating entry point
     for _ in range(2):                                 # two calls in a row
