@@ -44,8 +44,13 @@
  *   the first split launch on that stream, grown when a larger one is needed,
  *   and kept until the process exits; while the stream is being captured into
  *   a CUDA graph nothing is allocated and a launch without a large enough
- *   workspace does not split.  Nothing else is allocated per call
- *   (gemm_ex_noalloc allocates nothing at all).
+ *   workspace does not split.  A tile-starved fp32-output GEMM whose K loop is
+ *   long may instead split K over the two CTAs of a cluster (chosen by the
+ *   planner, or forced with SMO_GEMM_SPLIT_K=0/1); that allocates nothing:
+ *   one CTA stores its partial of each output plainly and the other adds its
+ *   own with a TMA reduce-add, so C receives exactly one rounding of the two
+ *   partials.  Nothing else is allocated per call (gemm_ex_noalloc allocates
+ *   nothing at all).
  *   Errors: every entry point returns GEMM_OK (0) or a negative gemm_status_t;
  *   argument errors launch nothing and leave C untouched.
  */
