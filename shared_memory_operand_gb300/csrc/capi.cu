@@ -350,7 +350,7 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
         // The owner streams the partials through the idle operand ring
         // (kFixRingBytes) in blocks of 128 accumulator columns.
         const bool fits = (size_t)pl.stages * pl.stage_stride >= smo::kFixRingBytes &&
-                          pl.BN % (32 * smo::kFixChunks) == 0;
+                          pl.BN % (32 * smo::kFixChunks) == 0 && !pl.tail;
         // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
         if (worth && fits && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
             const size_t work_bytes = (size_t)maxc * (size_t)pl.tile_m * (size_t)pl.BN * sizeof(float);
@@ -552,7 +552,8 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     const bool a_fused = pl->a.mn_major && pl->a.nbox > 1 && M % aT == 0 && pl->a.tile_mn % aT == 0 &&
                          encode_fused(&ta, in_dtype, A, M, K, batch, lda, strideA, pl->a.nbox, aT,
                                       (uint32_t)pl->bk) == GEMM_OK;
-    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % bT == 0 && pl->b.tile_mn % bT == 0 &&
+    // (a tiling with a narrower tail has B column origins off the box grid)
+    const bool b_fused = pl->b.mn_major && pl->b.nbox > 1 && N % bT == 0 && pl->b.tile_mn % bT == 0 && !pl->tail &&
                          encode_fused(&tb, in_dtype, B, N, K, batch, ldb, strideB, pl->b.nbox, bT,
                                       (uint32_t)pl->bk) == GEMM_OK;
     if ((!a_fused &&

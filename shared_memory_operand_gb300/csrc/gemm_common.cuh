@@ -32,6 +32,27 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int64_t t, int& b,
     nb = rr / gsz;
 }
 
+// Tile id -> (batch, m block, first column, width), with the tail region of a
+// wide tiling: tiles [tail_start, total_tiles) are tail_bn wide and cover M
+// blocks [tail_m0, tail_m0 + tail_gsz) x columns [tail_n0, N), in column
+// blocks of tail_gsz tiles.  Tiles before tail_start decode as decode_tile
+// does (the tail region is the end of the last M group's grouped order).
+__device__ __forceinline__ void decode_tile_w(const KParams& p, int64_t t, int& b, int& mb, int32_t& n0,
+                                              int32_t& bn) {
+    if (t >= p.tail_start) {
+        const int32_t r = (int32_t)(t - p.tail_start);
+        b = 0;
+        mb = p.tail_m0 + r % p.tail_gsz;
+        n0 = p.tail_n0 + (r / p.tail_gsz) * p.tail_bn;
+        bn = p.tail_bn;
+        return;
+    }
+    int nb;
+    decode_tile(p, t, b, mb, nb);
+    n0 = nb * p.BN;
+    bn = p.BN;
+}
+
 // One TMA load of a pipeline stage, owned by one lane of the producer warp.
 // All of a stage's loads (A boxes, then B boxes) are issued by consecutive
 // lanes in a single instruction: the producer's issue cost is then one
@@ -427,11 +448,12 @@ __device__ __forceinline__ void epi_store_partial(const KParams& p, int lane, in
 template <int OUT, typename Release>
 __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
                                               uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
-                                              int32_t m0, int32_t n0, int b, Release release) {
+                                              int32_t m0, int32_t n0, int b, Release release,
+                                              int chunks, int last_cols) {
     constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
-    for (int c = 0; c < p.epi_chunks; ++c) {
-        const bool last = c == p.epi_chunks - 1;
-        const bool partial = last && p.epi_last_cols < kChunkCols;
+    for (int c = 0; c < chunks; ++c) {
+        const bool last = c == chunks - 1;
+        const bool partial = last && last_cols < kChunkCols;
         const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
         if (!partial) {
             if (lane == 0) bulk_wait_read<1>();    // this slab's previous store has read it
@@ -445,7 +467,7 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
             if (lane == 0) release();
         }
         if (partial) {
-            epi_store_partial<OUT>(p, lane, m0, n0 + c * kChunkCols, p.epi_last_cols, b, v);
+            epi_store_partial<OUT>(p, lane, m0, n0 + c * kChunkCols, last_cols, b, v);
         } else {
             epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
             sbuf ^= 1u;
@@ -544,6 +566,16 @@ __device__ __forceinline__ bool epilogue_split_tile(const KParams& p, const CUte
 // first (128 per thread, packed), the accumulator is released, and only then
 // are the chunks staged and stored -- the MMA issuer waits for four tensor
 // memory reads instead of four whole chunk round trips.
+// The tile of the launch's main width (p.epi_chunks chunks, the last one
+// holding p.epi_last_cols columns).
+template <int OUT, typename Release>
+__device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
+                                              uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
+                                              int32_t m0, int32_t n0, int b, Release release) {
+    epilogue_tile<OUT>(p, tmC, tmem_acc, lane_field, slabs, sbuf, lane, m0, n0, b, release, p.epi_chunks,
+                       p.epi_last_cols);
+}
+
 // PARTIAL = 1: a tile of 193 .. 255 columns (4 chunks, the last one holding
 // p.epi_last_cols < 64 of them), whose last chunk is stored directly.
 template <int OUT, int PARTIAL, typename Release>

@@ -112,7 +112,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t budget = p.timeout_ns;
     const int64_t cluster_id = blockIdx.x >> 1;
     const int64_t nclusters = gridDim.x >> 1;
-    const int32_t half_bn = p.BN / 2;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
@@ -133,11 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             WorkItem w;
             work_begin(p, cluster_id, nclusters, wi);
             while (ok && work_next(p, wi, w)) {
-                int b, mb, nb;
-                decode_tile(p, w.tile, b, mb, nb);
+                int b, mb;
+                int32_t n0, tbn;
+                decode_tile_w(p, w.tile, b, mb, n0, tbn);
                 // this CTA's A rows / B columns
                 const int32_t mn0 = slot.is_a ? mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM)
-                                              : nb * p.BN + (int32_t)rank * half_bn;
+                                              : n0 + (int32_t)rank * (tbn / 2);
                 for (int kb = w.kb0; kb < w.kb1; kb += KG) {
                     const bool two = KG == 2 && kb + 1 < w.kb1;   // a range's last group may hold one block
                     int good = 1;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t a_desc0 = p.a_desc_hi | (uint64_t)((base >> 4) & 0x3FFFu);
             const uint64_t b_desc0 = p.b_desc_hi | (uint64_t)(((base + p.b_off) >> 4) & 0x3FFFu);
             const uint64_t ak = p.a_kstep >> 4, bk = p.b_kstep >> 4;
-            const uint32_t idesc = p.idesc;
+            const uint32_t idesc_main = p.idesc;
             uint32_t g = 0, ph = 0;
             uint64_t so = 0;                                                 // group's descriptor offset
             uint32_t it = 0;
@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + buf * (uint32_t)p.BN;
+                const uint32_t idesc = w.tile >= p.tail_start ? p.tail_idesc : idesc_main;   // tile width
                 for (int kb = w.kb0; kb < w.kb1; kb += KG) {
                     if (!mbar_wait(full_bar(g), ph, budget)) {
                         report_error(p.err, DEV_TIMEOUT_MMA);
@@ -283,8 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             return (((int64_t)rank * MSUB + i) * kEpiWarps + (int64_t)q) * kEpiRowsPerWarp * p.BN;
         };
         for (; work_next(p, wi, w); ++it) {
-            int b, mb, nb;
-            decode_tile(p, w.tile, b, mb, nb);
+            int b, mb;
+            int32_t n0, tbn;
+            decode_tile_w(p, w.tile, b, mb, n0, tbn);
+            const bool tail = w.tile >= p.tail_start;
+            const int chunks = tail ? p.tail_epi_chunks : p.epi_chunks;
+            const int last_cols = tail ? p.tail_epi_last_cols : p.epi_last_cols;
             const uint32_t buf = WIDE ? 0u : (it & 1u), aph = WIDE ? (it & 1u) : ((it >> 1) & 1u);
             int good = 1;
             if (lane == 0) good = mbar_wait(accf_bar(buf), aph, budget) ? 1 : 0;
@@ -346,21 +351,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
                                    (int32_t)q * kEpiRowsPerWarp;
                 if constexpr (WIDE && OUT != OUT_F32) {
-                    if (i == MSUB - 1 && (WIDE == 2 || p.BN == 256)) {
+                    if (i == MSUB - 1 && (WIDE == 2 || tbn == 256)) {
                         // the single accumulator: hand it back to the MMA issuer
                         // as soon as the last region sits in registers (four
                         // whole 64-column chunks; a narrower wide tile takes
                         // the chunk-by-chunk path below)
                         epilogue_region_early_release<OUT, WIDE == 2>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
-                                                           sbuf, lane, m0, nb * p.BN, b,
+                                                           sbuf, lane, m0, n0, b,
                                                            [&] { mbar_arrive_cluster(acce); });
                         continue;
                     }
                 }
-                epilogue_tile<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs, sbuf, lane, m0, nb * p.BN,
-                                   b, [&] {
+                epilogue_tile<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs, sbuf, lane, m0, n0, b,
+                                   [&] {
                                        if (i == MSUB - 1) mbar_arrive_cluster(acce);
-                                   });
+                                   },
+                                   chunks, last_cols);
             }
         }
         if (lane == 0) bulk_wait<0>();

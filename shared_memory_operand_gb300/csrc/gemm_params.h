@@ -79,6 +79,14 @@ struct KParams {
     int64_t sk_units;
     float* sk_work;                 // one fp32 partial-accumulator slot per cluster
     int32_t* sk_flags;              // per stream-K tile: epilogue warps that published
+    // Narrower tiles for the last, partial wave (CTA-pair wide kernel): tiles
+    // [tail_start, total_tiles) cover M blocks [tail_m0, tail_m0 + tail_gsz)
+    // x columns [tail_n0, N) with tiles tail_bn wide, so that they fit one
+    // wave; tail_start >= total_tiles: every tile is BN wide.
+    int64_t tail_start;
+    int32_t tail_m0, tail_gsz, tail_n0, tail_bn;
+    uint32_t tail_idesc;
+    int32_t tail_epi_chunks, tail_epi_last_cols;
     // Split-K over a 2-CTA cluster (one-CTA kernel, fp32 output): the CTA of
     // cluster rank 0 takes K blocks [0, split_kh), rank 1 [split_kh, num_k);
     // 0 = no split.

@@ -282,6 +282,40 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.num_m = (int)((M + p.tile_m - 1) / p.tile_m);
     p.num_n = (int)((N + bn - 1) / bn);
     p.tiles = tiles_for(p.tile_m, bn);
+    p.group_m = std::min(p.pair ? 8 : 16, p.num_m);
+    // Tail of a wide tiling (256 wide, one problem): when the tiles leave a
+    // last wave only partly full and those tiles, in the grouped order, are
+    // the last q N blocks of the last M group, they are re-tiled with the
+    // narrowest width (a multiple of 16 that keeps the TMA coordinate rule)
+    // whose tiles still fit one wave: 8192^2 has 6 full waves of 76 tiles and
+    // 56 left over (8 M blocks x 7 N blocks); as 72 tiles of 512 x 208 the
+    // last wave takes 13/16 of a full one.
+    if (p.wide && bn == 256 && batch == 1 && force != 1024 && wide_bn == 0) {
+        const int64_t C = clusters;
+        const int64_t T = p.tiles;
+        const int64_t R = T % C;
+        const int gstart = ((p.num_m - 1) / p.group_m) * p.group_m;
+        const int gsz = p.num_m - gstart;
+        if (T / C >= 1 && R > 0 && R % gsz == 0 && R / gsz < p.num_n) {
+            const int q = (int)(R / gsz);
+            const int64_t n0 = (int64_t)(p.num_n - q) * bn;
+            const int64_t cols = N - n0;
+            const int64_t per_m = C / gsz;                    // tail N blocks that fit the wave
+            for (int w = 16; w < bn; w += 16) {
+                if (b_major && ((w / 2) * p.in_es) % 16 != 0) continue;
+                if ((cols + w - 1) / w > per_m) continue;
+                p.tail = 1;
+                p.tail_bn = w;
+                p.tail_m0 = gstart;
+                p.tail_gsz = gsz;
+                p.tail_n0 = (int)n0;
+                p.tail_start = T - R;
+                p.tail_tiles = (int)(gsz * ((cols + w - 1) / w));
+                break;
+            }
+        }
+        if (p.tail) p.tiles = p.tail_start + p.tail_tiles;
+    }
     if (p.split) {
         // one tile per cluster (the epilogue stages in the idle operand ring)
         if (2 * p.tiles >= (1ll << 31)) {
@@ -293,8 +327,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     } else {
         p.grid = p.pair ? (int)(2 * std::min<int64_t>(p.tiles, clusters)) : (int)std::min<int64_t>(p.tiles, p.num_sms);
     }
-    p.group_m = std::min(p.pair ? 8 : 16, p.num_m);
     p.idesc = make_idesc(in_dtype, a_major, b_major, p.pair ? 2 * kBM : kBM, bn);
+    if (p.tail) p.tail_idesc = make_idesc(in_dtype, a_major, b_major, 2 * kBM, p.tail_bn);
 
     // Per-CTA operand tiles: A 128 rows (256 in a wide pair); B all BN columns,
     // or half of them in a pair.
@@ -312,7 +346,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     auto x_aligned = [](int64_t elems, int es) { return (elems * es) % 16 == 0; };
     const bool a_ok = !a_major || (x_aligned(p.tile_m, p.in_es) && x_aligned(p.a.tile_mn, p.in_es));
     const bool b_ok = !b_major || (x_aligned(bn, p.in_es) && x_aligned(p.b.tile_mn, p.in_es));
-    const bool c_ok = x_aligned(bn, out_dtype == 2 ? 4 : 2);
+    const bool c_ok = x_aligned(bn, out_dtype == 2 ? 4 : 2) &&
+                      (!p.tail || (x_aligned(p.tail_bn, out_dtype == 2 ? 4 : 2) && x_aligned(p.tail_n0, out_dtype == 2 ? 4 : 2) &&
+                                   (!b_major || (x_aligned(p.tail_bn / 2, p.in_es) && x_aligned(p.tail_n0, p.in_es)))));
     if (!a_ok || !b_ok || !c_ok) {
         p.why = "tile width breaks the 16-byte TMA coordinate rule";
         return p;
@@ -322,6 +358,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.c.chunk_cols = 128 / p.c.out_es;
     p.c.chunks = (bn + p.c.chunk_cols - 1) / p.c.chunk_cols;
     p.c.last_cols = bn - (p.c.chunks - 1) * p.c.chunk_cols;
+    if (p.tail) {
+        p.tail_chunks = (p.tail_bn + p.c.chunk_cols - 1) / p.c.chunk_cols;
+        p.tail_last_cols = p.tail_bn - (p.tail_chunks - 1) * p.c.chunk_cols;
+    }
     for (int i = 0; i < 5; ++i) p.c.basis_row[i] = epi_offset(1u << i, 0);
     for (int i = 0; i < 3; ++i) p.c.basis_chunk[i] = epi_offset(0, 1u << i);
     {
@@ -422,6 +462,14 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->epi_chunks = p.c.chunks;
     kp->epi_last_cols = p.c.last_cols;
     kp->split_kh = p.split ? p.split_kh : 0;
+    kp->tail_start = p.tail ? p.tail_start : p.tiles;
+    kp->tail_m0 = p.tail_m0;
+    kp->tail_gsz = p.tail_gsz;
+    kp->tail_n0 = p.tail_n0;
+    kp->tail_bn = p.tail_bn;
+    kp->tail_idesc = p.tail_idesc;
+    kp->tail_epi_chunks = p.tail_chunks;
+    kp->tail_epi_last_cols = p.tail_last_cols;
 }
 
 std::string describe_json(const Plan& p) {
@@ -444,7 +492,10 @@ std::string describe_json(const Plan& p) {
     o << "{\"ok\":" << (p.ok ? "true" : "false") << ",\"why\":\"" << p.why << "\""
       << ",\"M\":" << p.M << ",\"N\":" << p.N << ",\"K\":" << p.K << ",\"batch\":" << p.batch
       << ",\"pair\":" << p.pair << ",\"wide\":" << p.wide << ",\"split\":" << p.split
-      << ",\"split_kh\":" << p.split_kh << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
+      << ",\"split_kh\":" << p.split_kh << ",\"tail\":" << p.tail << ",\"tail_start\":" << p.tail_start
+      << ",\"tail_m0\":" << p.tail_m0 << ",\"tail_gsz\":" << p.tail_gsz << ",\"tail_n0\":" << p.tail_n0
+      << ",\"tail_bn\":" << p.tail_bn << ",\"tail_tiles\":" << p.tail_tiles << ",\"tail_idesc\":" << p.tail_idesc
+      << ",\"tail_chunks\":" << p.tail_chunks << ",\"tail_last_cols\":" << p.tail_last_cols << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
       << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads

@@ -54,6 +54,13 @@ struct Plan {
     int pair = 0;                   // 1: CTA pair (cta_group::2), 256 x BN tiles over two SMs
     int wide = 0;                   // 1 (pair only): 512 x 256 tiles, 256 A rows per CTA, one accumulator
     int split = 0;                  // 1 (one CTA, fp32 out): split-K over a 2-CTA cluster, one tile per cluster
+    // Tail (wide CTA pair, BN = 256): the last partial wave's tiles re-tiled
+    // tail_bn wide: M blocks [tail_m0, tail_m0 + tail_gsz) x columns [tail_n0, N)
+    int tail = 0;
+    int64_t tail_start = 0;
+    int tail_m0 = 0, tail_gsz = 0, tail_n0 = 0, tail_bn = 0, tail_tiles = 0;
+    uint32_t tail_idesc = 0;
+    int tail_chunks = 0, tail_last_cols = 0;
     int split_kh = 0;               // K blocks of the cluster's rank-0 CTA
     int tile_m = 128;               // output rows per tile (128; 256 for a pair; 512 for a wide pair)
     int BN = 256, stages = 4;

@@ -5,6 +5,7 @@ with the oracle's independent restatement and bank simulator."""
 import os
 import re
 
+import numpy as np
 import pytest
 
 import shared_memory_operand_gb300 as smo
@@ -270,7 +271,8 @@ def test_tile_choice_and_grid(lib):
     assert not d["split"] and d["BN"] == 128 and d["grid"] == 4
     # long K: the wide pair (512 x 256 tiles); short K: 256 x 256
     d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
-    assert d["pair"] and d["wide"] and d["BM"] == 512 and d["BN"] == 256 and d["tiles"] == 16 * 32
+    assert d["pair"] and d["wide"] and d["BM"] == 512 and d["BN"] == 256
+    assert d["tiles"] == 6 * 76 + 72 and d["tail"] and d["tail_bn"] == 208        # see test_wide_tail_*
     assert d["grid"] == 152 and d["stages"] == 4 and d["A"]["tile_mn"] == 256 and d["B"]["tile_mn"] == 128
     d = smo.gemm_plan_describe(16384, 8192, 1024, 0, 1, "bf16", "bf16")
     assert d["pair"] and not d["wide"] and d["BM"] == 256 and d["tiles"] == 64 * 32
@@ -355,6 +357,60 @@ def test_tma_coordinate_rule_refuses_unaligned_widths(lib, monkeypatch):
             if d["ok"]:
                 assert (d["BN"] * es) % 16 == 0 and (d["B"]["tile_mn"] * es) % 16 == 0
                 assert (d["A"]["tile_mn"] * es) % 16 == 0
+
+
+def _tiles_of(d):
+    """The output rectangles of a plan's tiles, decoded as the wide CTA-pair
+    kernel decodes them: tiles before tail_start in groups of group_m M blocks,
+    column-major inside a group; the tail region in column blocks of tail_gsz
+    tiles, tail_bn wide."""
+    BM, BN, gm = d["BM"], d["BN"], d["group_m"]
+    num_m, num_n = d["num_m"], d["num_n"]
+    out = []
+    for t in range(d["tiles"]):
+        if d["tail"] and t >= d["tail_start"]:
+            r = t - d["tail_start"]
+            mb = d["tail_m0"] + r % d["tail_gsz"]
+            n0 = d["tail_n0"] + (r // d["tail_gsz"]) * d["tail_bn"]
+            out.append((mb * BM, n0, d["tail_bn"]))
+            continue
+        span = gm * num_n
+        g = t // span
+        first = g * gm
+        gsz = min(num_m - first, gm)
+        rr = t - g * span
+        out.append(((first + rr % gsz) * BM, (rr // gsz) * BN, BN))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,bm,ind", [(8192, 8192, 8192, 1, "bf16"), (8192, 8192, 8192, 0, "bf16"),
+                                          (8192, 8192, 8192, 1, "e4m3"), (4096, 6912, 3072, 1, "bf16"),
+                                          (6144, 4608, 3072, 0, "bf16"), (6144, 6144, 3072, 1, "f16")])
+def test_wide_tail_covers_the_output_once(lib, M, N, K, bm, ind):
+    """The last, partial wave of a 256-wide wide tiling is re-tiled narrower:
+    the tiles (main ones up to tail_start, then the tail's) cover every
+    output element exactly once, the tail fits one wave of 76 clusters, the
+    main tiles fill whole waves, and the tail width keeps the TMA rule."""
+    d = smo.gemm_plan_describe(M, N, K, 0, bm, ind, "bf16")
+    assert d["ok"] and d["wide"] and d["tail"], d
+    assert d["tail_start"] % 76 == 0 and d["tail_tiles"] <= 76 and d["tail_bn"] < 256
+    es = 1 if ind == "e4m3" else 2
+    if bm:
+        assert (d["tail_bn"] // 2 * es) % 16 == 0 and (d["tail_n0"] * es) % 16 == 0
+    x = d["tail_idesc"]
+    assert ((x >> 17) & 63) * 8 == d["tail_bn"] and ((x >> 24) & 31) * 16 == 256
+    cover = np.zeros((-(-M // 512) * 512, N + 256), dtype=np.int8)
+    for (m0, n0, w) in _tiles_of(d):
+        cover[m0:m0 + 512, n0:n0 + w] += 1
+    assert np.all(cover[:M, :N] == 1)
+
+
+def test_wide_tail_off_when_forced_or_full(lib, monkeypatch):
+    d = smo.gemm_plan_describe(4096, 4096, 4096, 0, 1, "bf16", "bf16")     # two full waves of 224
+    assert not d["tail"]
+    monkeypatch.setenv("SMO_GEMM_WIDE_BN", "256")
+    d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")     # uniform 512 x 256
+    assert not d["tail"] and d["tiles"] == 16 * 32
 
 
 def test_pair_descriptors(lib, monkeypatch):

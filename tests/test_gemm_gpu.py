@@ -488,3 +488,17 @@ def test_wide_tile_widths(wbn, am, bm, monkeypatch):
         plan = smo.gemm_plan_describe(M, N, K, am, bm, ind, out, batch)
         assert plan["wide"] == 1 and plan["BN"] == wbn
         _full(p, exact=(dist == "int"))
+
+
+@pytest.mark.parametrize("M,N,K,bm,ind,out,dist", [
+    (4096, 6912, 3072, MN_MAJOR, "bf16", "bf16", "uniform"),     # tail of 72 tiles, 240 wide
+    (6144, 4608, 3072, K_MAJOR, "bf16", "f32", "normal"),        # 76 tiles, 224 wide, fp32 out
+    (6144, 6144, 3072, MN_MAJOR, "f16", "f16", "int"),           # 208 wide (partial 16-column chunk), exact
+])
+def test_wide_tail_full_compare(M, N, K, bm, ind, out, dist):
+    """The last partial wave of a 512 x 256 tiling re-tiled narrower (its own
+    instruction descriptor, B columns and epilogue chunks per tile)."""
+    plan = smo.gemm_plan_describe(M, N, K, K_MAJOR, bm, ind, out)
+    assert plan["tail"] == 1
+    p = make_problem(M, N, K, a_major=K_MAJOR, b_major=bm, in_dtype=ind, out_dtype=out, dist=dist, seed=M + N)
+    _full(p, exact=(dist == "int"))
