@@ -108,6 +108,12 @@ int wide_bn_from_env() {
     return (v >= 16 && v <= 256 && v % 16 == 0) ? v : 0;
 }
 
+// Serpentine K order of wide tiles (on unless SMO_GEMM_SERPENTINE=0).
+int serpentine_from_env() {
+    const char* s = std::getenv("SMO_GEMM_SERPENTINE");
+    return (s && s[0] == '0') ? 0 : 1;
+}
+
 // Split-K policy of the one-CTA kernel: SMO_GEMM_SPLIT_K=0 never, =1 whenever
 // the plan allows it, unset = the planner's choice (tile-starved problems).
 int split_k_from_env() {
@@ -577,6 +583,7 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     kp.timeout_ns = g_timeout_ns.load();
     kp.stall = g_stall.load();
     kp.kgroup = kgroup_from_env(kp.kgroup, kp.stages, pl->pair);
+    kp.serp = pl->wide ? serpentine_from_env() : 0;
     kp.group_m = group_m_from_env(kp.group_m, kp.num_m);
 
     switch (out_dtype) {

@@ -131,14 +131,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             WorkIter wi;
             WorkItem w;
             work_begin(p, cluster_id, nclusters, wi);
-            while (ok && work_next(p, wi, w)) {
+            for (uint32_t tix = 0; ok && work_next(p, wi, w); ++tix) {
                 int b, mb;
                 int32_t n0, tbn;
                 decode_tile_w(p, w.tile, b, mb, n0, tbn);
                 // this CTA's A rows / B columns
                 const int32_t mn0 = slot.is_a ? mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM)
                                               : n0 + (int32_t)rank * (tbn / 2);
+                // Wide tiles (one stage per barrier pair): every other tile of
+                // this cluster loads its K blocks last to first.  A wave then
+                // begins on the K slices of A the previous wave read last,
+                // which are the ones still in L2.  The MMAs consume the
+                // stages in ring order either way (only the summation order
+                // changes).
+                const bool rev = KG == 1 && p.serp && (tix & 1u);
                 for (int kb = w.kb0; kb < w.kb1; kb += KG) {
+                    const int kload = rev ? w.kb0 + w.kb1 - 1 - kb : kb;
                     const bool two = KG == 2 && kb + 1 < w.kb1;   // a range's last group may hold one block
                     int good = 1;
                     if (lane == 0) good = mbar_wait(empty_bar(g), ph ^ 1u, budget) ? 1 : 0;
@@ -159,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp(lmask);
                         int32_t c0, c1, c2;
-                        slot_coords(slot, mn0, kb * p.bk, c0, c1, c2);
+                        slot_coords(slot, mn0, kload * p.bk, c0, c1, c2);
                         tma_load_4d_pair(gst + slot.dst_off, slot.tm, fb, c0, c1, c2, b);
                         if (two) {
                             slot_coords(slot, mn0, (kb + 1) * p.bk, c0, c1, c2);

@@ -83,6 +83,10 @@ struct KParams {
     // [tail_start, total_tiles) cover M blocks [tail_m0, tail_m0 + tail_gsz)
     // x columns [tail_n0, N) with tiles tail_bn wide, so that they fit one
     // wave; tail_start >= total_tiles: every tile is BN wide.
+    // Wide tiles: a cluster's odd-numbered tiles run their K loop from the
+    // last K block down (1 = on), so that a wave starts on the K slices the
+    // previous wave used last, still in L2.
+    int32_t serp;
     int64_t tail_start;
     int32_t tail_m0, tail_gsz, tail_n0, tail_bn;
     uint32_t tail_idesc;
