@@ -35,8 +35,8 @@ struct DevState {
     int32_t* d_err = nullptr;
     bool attr_set[12] = {};         // one-CTA kernels: [(KIND * 3 + OUT) * 2 + KG - 1]
     bool split_attr_set[4] = {};    // split-K one-CTA kernels (fp32 out): [KIND * 2 + KG - 1]
-    bool pair_attr_set[18] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT], WIDE 0..2
-    int pair_max_clusters[18] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
+    bool pair_attr_set[12] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT]
+    int pair_max_clusters[12] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
     // Stream-K workspace, one per stream so that GEMMs running concurrently
     // on different streams never share partial slots or tile counters.
     struct SkWork {
@@ -313,7 +313,7 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
     // the prologue may overlap the previous kernel (see launch_single_kg)
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.blockDim = dim3(smo::kThreads, 1, 1);
+    cfg.blockDim = dim3(WIDE ? smo::kWideThreads : smo::kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -355,8 +355,9 @@ int launch_pair(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUten
         const bool worth = stream_k == 1 || (!pl.wide && (sk_tiles * (int64_t)pl.num_k) / maxc >= 48);
         // The owner streams the partials through the idle operand ring
         // (kFixRingBytes) in blocks of 128 accumulator columns.
+        // (wide tiles are never split: their 8-warp epilogue has no fix-up)
         const bool fits = (size_t)pl.stages * pl.stage_stride >= smo::kFixRingBytes &&
-                          pl.BN % (32 * smo::kFixChunks) == 0 && !pl.tail;
+                          pl.BN % (32 * smo::kFixChunks) == 0 && !pl.tail && !pl.wide;
         // at most 32 pieces per tile (a tile spans about maxc / sk_tiles + 1 clusters)
         if (worth && fits && sk_tiles > 0 && (maxc + sk_tiles - 1) / sk_tiles + 1 <= 32) {
             const size_t work_bytes = (size_t)maxc * (size_t)pl.tile_m * (size_t)pl.BN * sizeof(float);
@@ -419,13 +420,8 @@ template <int OUT, int KIND>
 int launch_kind(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KParams& kp, cudaStream_t stream, int stream_k) {
     if (!pl.pair) return launch_single<OUT, KIND>(pl, ds, ta, tb, tc, kp, stream);
-    if (!pl.wide) return launch_pair<OUT, KIND, 0>(pl, ds, ta, tb, tc, kp, stream, stream_k);
-    if constexpr (OUT != smo::OUT_F32) {
-        // 193 .. 255 columns: the variant with a partial last chunk
-        if (pl.c.chunks == 4 && pl.c.last_cols < 64)
-            return launch_pair<OUT, KIND, 2>(pl, ds, ta, tb, tc, kp, stream, stream_k);
-    }
-    return launch_pair<OUT, KIND, 1>(pl, ds, ta, tb, tc, kp, stream, stream_k);
+    return pl.wide ? launch_pair<OUT, KIND, 1>(pl, ds, ta, tb, tc, kp, stream, stream_k)
+                   : launch_pair<OUT, KIND, 0>(pl, ds, ta, tb, tc, kp, stream, stream_k);
 }
 
 template <int OUT>

@@ -355,6 +355,24 @@ __device__ __forceinline__ void epi_load_chunk(uint32_t tmem_acc, uint32_t lane_
     }
 }
 
+// Step 1 for 16-bit output with fewer registers: the chunk's two 32-column
+// halves are read and packed one after the other (32 raw values live at a
+// time instead of 64), for a warp that holds a whole accumulator in
+// registers.
+template <int OUT>
+__device__ __forceinline__ void epi_load_chunk_halves(uint32_t tmem_acc, uint32_t lane_field, int c,
+                                                      uint32_t (&v)[32]) {
+    static_assert(OUT != OUT_F32, "16-bit output");
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_acc + lane_field + (uint32_t)(c * 64 + h * 32), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * h + i] = pack2<OUT>(r[2 * i], r[2 * i + 1]);
+    }
+}
+
 // Step 2: stage the chunk in this warp's swizzled slab and store it with TMA
 // (the ragged < 16-byte end of a row is copied from the slab directly).  The
 // caller has made sure the slab's previous store has finished reading it.
@@ -475,6 +493,16 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
     }
 }
 
+// The tile of the launch's main width (p.epi_chunks chunks, the last one
+// holding p.epi_last_cols columns).
+template <int OUT, typename Release>
+__device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
+                                              uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
+                                              int32_t m0, int32_t n0, int b, Release release) {
+    epilogue_tile<OUT>(p, tmC, tmem_acc, lane_field, slabs, sbuf, lane, m0, n0, b, release, p.epi_chunks,
+                       p.epi_last_cols);
+}
+
 // Split-K epilogue of one warp (fp32 output; one tile per 2-CTA cluster, the
 // two CTAs holding the partial sums of the two halves of K).  The tile's
 // column chunks are shared out: CTA rank 0 owns chunks [0, h), rank 1 chunks
@@ -561,47 +589,80 @@ __device__ __forceinline__ bool epilogue_split_tile(const KParams& p, const CUte
     return true;
 }
 
-// The last accumulator region of a tile with 16-bit output and 256 columns
-// (4 chunks): all four chunks are read from tensor memory into registers
-// first (128 per thread, packed), the accumulator is released, and only then
-// are the chunks staged and stored -- the MMA issuer waits for four tensor
-// memory reads instead of four whole chunk round trips.
-// The tile of the launch's main width (p.epi_chunks chunks, the last one
-// holding p.epi_last_cols columns).
+// Epilogue of a wide tile (two 128-row accumulator regions per CTA) for one
+// of its 8 warps: TMEM lane quarter `lane_field`, chunks [c0, c0 + nc) of
+// each region (its half of the tile's columns).
+//   16-bit output: the warp reads its (at most 2 + 2) chunks of both regions
+//     from tensor memory into registers (128 per thread, packed), hands the
+//     accumulator back -- the MMA issuer starts the next tile at once -- and
+//     then stores the chunks through its slab while the next tile's MMAs run.
+//   fp32 output (twice the registers): chunk by chunk, the accumulator handed
+//     back after the warp's last tensor-memory read.
+// A partial last chunk (tile width not a multiple of the chunk) is stored
+// directly.  mrow: the warp's first row in region 0 (region 1 is 128 below).
 template <int OUT, typename Release>
-__device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
-                                              uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
-                                              int32_t m0, int32_t n0, int b, Release release) {
-    epilogue_tile<OUT>(p, tmC, tmem_acc, lane_field, slabs, sbuf, lane, m0, n0, b, release, p.epi_chunks,
-                       p.epi_last_cols);
-}
-
-// PARTIAL = 1: a tile of 193 .. 255 columns (4 chunks, the last one holding
-// p.epi_last_cols < 64 of them), whose last chunk is stored directly.
-template <int OUT, int PARTIAL, typename Release>
-__device__ __forceinline__ void epilogue_region_early_release(const KParams& p, const CUtensorMap* tmC,
-                                                              uint32_t tmem_acc, uint32_t lane_field,
-                                                              uint32_t slabs, uint32_t& sbuf, int lane, int32_t m0,
-                                                              int32_t n0, int b, Release release) {
-    static_assert(OUT != OUT_F32, "16-bit output: 64 columns per chunk");
-    constexpr int kChunks = 4;                      // 256 columns
-    uint32_t v[kChunks][32];
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c)
-        epi_load_chunk<OUT>(tmem_acc, lane_field, c, v[c]);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) release();
-#pragma unroll
-    for (int c = 0; c < kChunks - PARTIAL; ++c) {
-        const uint32_t slab = slabs + sbuf * kEpiSlabBytes;
-        if (lane == 0) bulk_wait_read<1>();
+__device__ __forceinline__ void epilogue_wide_warp(const KParams& p, const CUtensorMap* tmC, uint32_t acc,
+                                                   uint32_t lane_field, uint32_t slab, int lane, int32_t mrow,
+                                                   int32_t n0, int b, int c0, int nc, int chunks, int last_cols,
+                                                   Release release) {
+    constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
+    if (nc <= 0) {                                  // a narrow tile may leave this warp nothing
         __syncwarp();
-        epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * 64, b, v[c]);
-        sbuf ^= 1u;
+        if (lane == 0) release();
+        return;
     }
-    if constexpr (PARTIAL)
-        epi_store_partial<OUT>(p, lane, m0, n0 + (kChunks - 1) * 64, p.epi_last_cols, b, v[kChunks - 1]);
+    if constexpr (OUT != OUT_F32) {
+        if (last_cols == kChunkCols) {
+            // whole chunks: everything into registers, hand back, then store
+            uint32_t v[2][2][32];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (j < nc) epi_load_chunk_halves<OUT>(acc + (uint32_t)(r * 256), lane_field, c0 + j, v[r][j]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (j < nc) {
+                        if (lane == 0) bulk_wait_read<0>();   // the slab's previous store has read it
+                        __syncwarp();
+                        epi_store_chunk<OUT>(p, tmC, slab, lane, mrow + r * kBM, n0 + (c0 + j) * kChunkCols, b,
+                                             v[r][j]);
+                    }
+                }
+            }
+            return;
+        }
+    }
+    // fp32 output (twice the registers), or a partial last chunk (the tail
+    // of a wide tiling): chunk by chunk, the accumulator handed back after the
+    // warp's last tensor-memory read.
+    for (int r = 0; r < 2; ++r) {
+        for (int j = 0; j < nc; ++j) {
+            const int c = c0 + j;
+            const int32_t m0 = mrow + r * kBM;
+            const bool partial = c == chunks - 1 && last_cols < kChunkCols;
+            if (!partial) {
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+            }
+            uint32_t v[32];
+            epi_load_chunk<OUT>(acc + (uint32_t)(r * 256), lane_field, c, v);
+            if (r == 1 && j == nc - 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) release();
+            }
+            if (partial)
+                epi_store_partial<OUT>(p, lane, m0, n0 + c * kChunkCols, last_cols, b, v);
+            else
+                epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
+        }
+    }
 }
 
 }  // namespace smo

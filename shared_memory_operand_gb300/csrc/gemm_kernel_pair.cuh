@@ -16,7 +16,9 @@
 //              8 MMAs: the single issuing thread, not the tensor pipe, set the
 //              pace with a wait and a commit per 4), two accumulators;
 //   512 x 256: 256 A rows per CTA in two 128-row halves with their own MMAs,
-//              4 stages of 48 KiB, one accumulator of 512 columns.
+//              4 stages of 48 KiB, one accumulator of 512 columns, 8
+//              epilogue warps (320 threads) that read the whole accumulator
+//              into registers and hand it back before storing.
 //
 // Synchronisation across the pair:
 //   full[g]    (even CTA only) -- both CTAs' TMA loads of the group complete
@@ -24,7 +26,8 @@
 //                                 the even producer arms it for both CTAs' bytes
 //   empty[g]   (both)          -- the MMA thread's commit multicasts to both
 //   acc_full   (both)          -- likewise, after the last K block of a tile
-//   acc_empty  (even CTA only) -- 4 epilogue warps of each CTA arrive
+//   acc_empty  (even CTA only) -- the epilogue warps of each CTA arrive (4, or 8
+//                                 for wide tiles)
 // Every wait is bounded; cluster barriers at start (barriers initialised,
 // tensor memory allocated) and end (no CTA leaves while its peer may still
 // signal it).
@@ -43,22 +46,20 @@ constexpr uint32_t kHalfABytes = kBM * kStageKBytes;   // 128 A rows of one stag
 // KIND: MmaKind (kind::f16 for 16-bit operands, kind::f8f6f4 for FP8).
 // WIDE: 0 -- 256 x 256 tiles, 128 A rows per CTA, two accumulators, stages
 //            handed over in groups of two (6 x 32 KiB);
-//       2 -- as 1, for tiles 193 .. 255 columns wide with 16-bit output: the
-//            last 64-column chunk is partial and stored directly, still after
-//            the early hand-back of the accumulator (a variant of its own, so
-//            that the 256-wide kernel keeps its registers);
-//       1 -- 512 x 256 tiles, 256 A rows per CTA (two 128-row halves, each
-//            with its own 256 x 256 MMAs into TMEM columns 0..255 / 256..511),
-//            one accumulator, one stage per barrier pair (4 x 48 KiB).  The B
-//            half-panel of a stage then feeds twice the MMAs: 47 instead of 64
-//            operand bytes per tensor cycle, so the same ring keeps more MMA
-//            work in flight.
+//       1 -- 512 x BN tiles (BN <= 256), 256 A rows per CTA (two 128-row
+//            halves, each with its own 256 x BN MMAs into TMEM columns
+//            0..BN-1 / 256..256+BN-1), one accumulator, one stage per barrier
+//            pair (4 x 48 KiB).  The B half-panel of a stage then feeds twice
+//            the MMAs: 47 instead of 64 operand bytes per tensor cycle, so the
+//            same ring keeps more MMA work in flight.  8 epilogue warps hand
+//            the single accumulator back as soon as it sits in registers
+//            (16-bit output); no stream-K.
 template <int OUT, int KIND, int WIDE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(WIDE ? kWideThreads : kThreads, 1)
     smo_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
-    static_assert(WIDE != 2 || OUT != OUT_F32, "partial-chunk variant: 16-bit output");
     constexpr int KG = WIDE ? 1 : kPairGroup;      // stages per full/empty barrier pair
+    constexpr int EPIW = WIDE ? kWideEpiWarps : kEpiWarps;   // epilogue warps per CTA
     constexpr int MSUB = WIDE ? 2 : 1;             // 128-row A halves (and accumulator regions) per CTA
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 2 * kEpiWarps);
+            mbar_init(acce_bar(b), 2 * EPIW);
         }
         mbar_init(drain_bar, 1);
         for (int j = 0; j < kEpiWarps * kFixBufs; ++j) mbar_init(fix_bar(j), 1);
@@ -278,6 +279,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(drain_bar, 0, budget)) report_error(p.err, DEV_TIMEOUT_TEARDOWN);
         }
         __syncwarp();
+    } else if constexpr (WIDE != 0) {
+        // ------------------------------------------------ epilogue, wide tiles (both CTAs, 8 warps)
+        // warp 2 + e: tensor-memory lane quarter warp % 4 (the warps a CTA
+        // may read a quarter with), column half e / 4; one staging slab each
+        const uint32_t e = (uint32_t)warp - 2u;
+        const uint32_t q = (uint32_t)warp & 3u;
+        const uint32_t h = e >> 2;
+        const uint32_t lane_field = (q * 32u) << 16;
+        const uint32_t slab = base + p.off_epi + e * kEpiSlabBytes;
+        uint32_t it = 0;
+        WorkIter wi;
+        WorkItem w;
+        work_begin(p, cluster_id, nclusters, wi);
+        for (; work_next(p, wi, w); ++it) {
+            int b, mb;
+            int32_t n0, tbn;
+            decode_tile_w(p, w.tile, b, mb, n0, tbn);
+            const bool tail = w.tile >= p.tail_start;
+            const int chunks = tail ? p.tail_epi_chunks : p.epi_chunks;
+            const int last_cols = tail ? p.tail_epi_last_cols : p.epi_last_cols;
+            int good = 1;
+            if (lane == 0) good = mbar_wait(accf_bar(0), it & 1u, budget) ? 1 : 0;
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                if (lane == 0) report_error(p.err, DEV_TIMEOUT_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acce = mapa_shared(acce_bar(0), lead);
+            const int half = (chunks + 1) / 2;
+            const int c0 = (int)h * half;
+            const int nc = min(chunks - c0, half);
+            // CTA `rank` holds tile rows rank * 256 .. (region 0) and + 128 (region 1)
+            const int32_t mrow = mb * (4 * kBM) + (int32_t)rank * (2 * kBM) + (int32_t)q * kEpiRowsPerWarp;
+            epilogue_wide_warp<OUT>(p, &tmC, tmem_base, lane_field, slab, lane, mrow, n0, b, c0, nc, chunks,
+                                    last_cols, [&] { mbar_arrive_cluster(acce); });
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
     } else {
         // ------------------------------------------------ epilogue (both CTAs)
         const uint32_t q = (uint32_t)warp & 3u;
@@ -358,18 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // CTA `rank`'s accumulator region i holds tile rows rank * 128 * MSUB + i * 128 ...
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +
                                    (int32_t)q * kEpiRowsPerWarp;
-                if constexpr (WIDE && OUT != OUT_F32) {
-                    if (i == MSUB - 1 && (WIDE == 2 || tbn == 256)) {
-                        // the single accumulator: hand it back to the MMA issuer
-                        // as soon as the last region sits in registers (four
-                        // whole 64-column chunks; a narrower wide tile takes
-                        // the chunk-by-chunk path below)
-                        epilogue_region_early_release<OUT, WIDE == 2>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs,
-                                                           sbuf, lane, m0, n0, b,
-                                                           [&] { mbar_arrive_cluster(acce); });
-                        continue;
-                    }
-                }
                 epilogue_tile<OUT>(p, &tmC, acc + (uint32_t)(i * 256), lane_field, slabs, sbuf, lane, m0, n0, b,
                                    [&] {
                                        if (i == MSUB - 1) mbar_arrive_cluster(acce);

@@ -366,8 +366,9 @@ def test_stream_k_tiles_full_compare(M, N, K, dist, monkeypatch):
     (1800, 1100, 700, "normal"),      # ragged M, N
 ])
 def test_stream_k_wide_tiles_full_compare(M, N, K, dist, monkeypatch):
-    """Stream-K on 512 x 256 tiles: each piece carries two accumulator regions
-    per CTA and every warp announces its partial once."""
+    """Stream-K forced on a 512 x 256 tiling: wide tiles are never split (their
+    8-warp epilogue has no fix-up), so the launch runs whole tiles -- still
+    every output, exactly."""
     monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
     monkeypatch.setenv("SMO_GEMM_STREAM_K", "1")
     p = make_problem(M, N, K, a_major=K_MAJOR, b_major=MN_MAJOR, dist=dist, seed=M + K + 1,
