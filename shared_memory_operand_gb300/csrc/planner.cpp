@@ -198,11 +198,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     const double cpair = (double)((tpair + clusters - 1) / clusters) * 0.85;
     // A wide pair tile is two pair tiles' work on three quarters of the
     // operand bytes (measured about 5% cheaper per flop at 8192^3), but its
-    // single accumulator leaves the epilogue exposed once per tile: it only
-    // wins when every tile runs a long K loop (measured: -19% at 16 K blocks,
-    // -6% at 32, +5% at 64, +7% at 128).
+    // single accumulator is held once per tile while the epilogue warps read
+    // it out: it wins when every tile runs a long enough K loop.  Measured
+    // with the 8-warp epilogue that hands the accumulator back from
+    // registers: 16 K blocks (skinny) -7%, 32 (batched) +1.8%.
     const double cwide = (double)((twide + clusters - 1) / clusters) * 1.62;
-    const bool long_k = p.num_k >= 48;
+    const bool long_k = p.num_k >= 32;
     int choice;
     if (force == 128 || force == 192 || force == 256 || force == 384 || force == 512 || force == 1024) choice = force;
     else if (cpair <= c256 && cpair <= c128) choice = (long_k && cwide < cpair) ? 1024 : 512;
@@ -258,10 +259,13 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     if (p.wide) {
         // Wave quantisation of wide tiles: a narrower tile (still a multiple
         // of 16 columns, so that each CTA's half is a whole number of 8-column
-        // core matrices) takes proportionally fewer tensor cycles, so a width
-        // whose tile count fills the last wave better can win: 4096^2 has 128
-        // tiles of 512 x 256 on 76 clusters (1.68 waves, run as 2), but 152 of
-        // 512 x 224 (exactly 2 waves of 7/8 the work each).  Ties keep 256.
+        // core matrices) takes fewer tensor cycles, so a width whose tile
+        // count fills the last wave better can win: 4096^2 has 128 tiles of
+        // 512 x 256 on 76 clusters (1.68 waves, run as 2), but 152 of 512 x
+        // 224 (exactly 2 waves).  A tile's time is modelled as 0.35 + 0.65 x
+        // width / 256 of a 256-wide one: its A panel, fill and epilogue do not
+        // shrink with the width (measured: 4096^3 +5% at 224, 8192^3's tail
+        // wave +1.4% at 208, 32 x 2048^3 -8% at 208).  Ties keep 256.
         if (wide_bn >= 16 && wide_bn <= 256 && wide_bn % 16 == 0) {
             bn = wide_bn;
         } else {
@@ -270,7 +274,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
                 // an N-major B half-tile must start on a 16-byte boundary (TMA)
                 if (b_major && ((w / 2) * p.in_es) % 16 != 0) continue;
                 const int64_t t = tiles_for(4 * kBM, w);
-                const double cost = (double)((t + clusters - 1) / clusters) * (double)w / 256.0;
+                const double cost = (double)((t + clusters - 1) / clusters) * (0.35 + 0.65 * (double)w / 256.0);
                 if (w == 256 || cost < best - 1e-9) {
                     best = cost;
                     bn = w;
