@@ -491,6 +491,21 @@ def test_wide_tile_widths(wbn, am, bm, monkeypatch):
         _full(p, exact=(dist == "int"))
 
 
+@pytest.mark.parametrize("K", [64, 128, 256, 320, 1000])
+@pytest.mark.parametrize("N,out", [(4608, "bf16"), (4192, "bf16"), (4608, "f32")])
+def test_wide_short_k_many_tiles(K, N, out, monkeypatch):
+    """Wide tiles with K loops shorter and longer than the 4-stage ring, several
+    tiles per cluster: the issuer runs a tile's region-0 MMAs on the stages
+    already loaded while region 1 of the previous tile is still being read,
+    then the region-1 MMAs; integers bit-exact."""
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "1024")
+    p = make_problem(8192, N, K, a_major=K_MAJOR, b_major=MN_MAJOR, in_dtype="bf16", out_dtype=out,
+                     dist="int", seed=K + N)   # N = 4608: 256-wide tiles; 4192: 224 (partial last chunk)
+    plan = smo.gemm_plan_describe(p.M, p.N, p.K, p.a_major, p.b_major, p.in_dtype, p.out_dtype)
+    assert plan["wide"] == 1 and plan["tiles"] > 2 * 76
+    _full(p, exact=True)
+
+
 @pytest.mark.parametrize("M,N,K,bm,ind,out,dist", [
     (4096, 6912, 3072, MN_MAJOR, "bf16", "bf16", "uniform"),     # tail of 72 tiles, 240 wide
     (6144, 4608, 3072, K_MAJOR, "bf16", "f32", "normal"),        # 76 tiles, 224 wide, fp32 out
