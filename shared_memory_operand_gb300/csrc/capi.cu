@@ -33,7 +33,7 @@ struct DevState {
     bool usable = false;
     int num_sms = 0;
     int32_t* d_err = nullptr;
-    bool attr_set[12] = {};         // one-CTA kernels: [(KIND * 3 + OUT) * 2 + KG - 1]
+    bool attr_set[24] = {};         // one-CTA kernels: [((KIND * 3 + OUT) * 2 + KG - 1) * 2 + EPI8]
     bool split_attr_set[4] = {};    // split-K one-CTA kernels (fp32 out): [KIND * 2 + KG - 1]
     bool pair_attr_set[12] = {};    // pair kernels: [(WIDE * 2 + KIND) * 3 + OUT]
     int pair_max_clusters[12] = {};   // co-resident 2-CTA clusters of each pair kernel (same index)
@@ -239,13 +239,14 @@ int encode_fused(CUtensorMap* m, int dt, const void* ptr, uint64_t mn, uint64_t 
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_UNSUPPORTED;
 }
 
-template <int OUT, int KG, int KIND, int SPLIT>
+template <int OUT, int KG, int KIND, int SPLIT, int EPI8>
 int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUtensorMap& tb,
                      const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
-    auto kern = smo::smo_gemm_kernel<OUT, KG, KIND, SPLIT>;
+    auto kern = smo::smo_gemm_kernel<OUT, KG, KIND, SPLIT, EPI8>;
     {
         std::lock_guard<std::mutex> lk(g_mu);     // once per device and kernel variant
-        bool& set = SPLIT ? ds.split_attr_set[KIND * 2 + KG - 1] : ds.attr_set[(KIND * 3 + OUT) * 2 + KG - 1];
+        bool& set = SPLIT ? ds.split_attr_set[KIND * 2 + KG - 1]
+                          : ds.attr_set[((KIND * 3 + OUT) * 2 + KG - 1) * 2 + EPI8];
         if (!set) {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo::kSmemLimit) !=
                 cudaSuccess) {
@@ -268,7 +269,7 @@ int launch_single_kg(const Plan& pl, DevState& ds, const CUtensorMap& ta, const 
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
-    cfg.blockDim = dim3(smo::kThreads, 1, 1);
+    cfg.blockDim = dim3(EPI8 ? smo::kWideThreads : smo::kThreads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -285,13 +286,20 @@ int launch_single(const Plan& pl, DevState& ds, const CUtensorMap& ta, const CUt
                   const CUtensorMap& tc, const KParams& kp, cudaStream_t stream) {
     if constexpr (OUT == smo::OUT_F32) {
         if (pl.split)
-            return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 1>(pl, ds, ta, tb, tc, kp, stream)
-                                  : launch_single_kg<OUT, 1, KIND, 1>(pl, ds, ta, tb, tc, kp, stream);
+            return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 1, 0>(pl, ds, ta, tb, tc, kp, stream)
+                                  : launch_single_kg<OUT, 1, KIND, 1, 0>(pl, ds, ta, tb, tc, kp, stream);
     } else {
         if (pl.split) return GEMM_ERR_UNSUPPORTED;     // the planner splits fp32 output only
     }
-    return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 0>(pl, ds, ta, tb, tc, kp, stream)
-                          : launch_single_kg<OUT, 1, KIND, 0>(pl, ds, ta, tb, tc, kp, stream);
+    // eight epilogue warps when every CTA has one tile, whose epilogue no
+    // next main loop hides, and each warp then holds at most two chunks
+    // (measured: 1500 x 1152 x 896 -0.1 to -1.7%, 256^3 -3%; with several
+    // tiles per CTA, or four chunks per warp, four warps are as fast or faster)
+    if (pl.tiles <= pl.grid && kp.epi_chunks <= 4)
+        return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 0, 1>(pl, ds, ta, tb, tc, kp, stream)
+                              : launch_single_kg<OUT, 1, KIND, 0, 1>(pl, ds, ta, tb, tc, kp, stream);
+    return kp.kgroup == 2 ? launch_single_kg<OUT, 2, KIND, 0, 0>(pl, ds, ta, tb, tc, kp, stream)
+                          : launch_single_kg<OUT, 1, KIND, 0, 0>(pl, ds, ta, tb, tc, kp, stream);
 }
 
 // CTA-pair kernel: clusters of two CTAs, one per SM; the persistent grid is

@@ -503,6 +503,67 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
                        p.epi_last_cols);
 }
 
+// One of eight epilogue warps of a one-CTA tile: tensor-memory lane quarter
+// `lane_field`, chunks [c0, c0 + nc) of the tile's `chunks` (the last one
+// holding `last_cols` columns), staged through the warp's one slab.  With at
+// most two chunks the warp reads both into registers and hands the
+// accumulator back before it stores them; with more it goes chunk by chunk
+// and hands back after its last tensor-memory read.
+template <int OUT, typename Release>
+__device__ __forceinline__ void epilogue_tile_part(const KParams& p, const CUtensorMap* tmC, uint32_t tmem_acc,
+                                                   uint32_t lane_field, uint32_t slab, int lane, int32_t m0,
+                                                   int32_t n0, int b, int c0, int nc, int chunks, int last_cols,
+                                                   Release release) {
+    constexpr int kChunkCols = (OUT == OUT_F32) ? 32 : 64;
+    if (nc <= 0) {                                  // a narrow tile may leave this warp nothing
+        __syncwarp();
+        if (lane == 0) release();
+        return;
+    }
+    if (nc <= 2) {
+        uint32_t v[2][32];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (j < nc) epi_load_chunk<OUT>(tmem_acc, lane_field, c0 + j, v[j]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) release();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (j < nc) {
+                const int c = c0 + j;
+                if (c == chunks - 1 && last_cols < kChunkCols) {
+                    epi_store_partial<OUT>(p, lane, m0, n0 + c * kChunkCols, last_cols, b, v[j]);
+                } else {
+                    if (lane == 0) bulk_wait_read<0>();   // the slab's previous store has read it
+                    __syncwarp();
+                    epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v[j]);
+                }
+            }
+        }
+        return;
+    }
+    for (int j = 0; j < nc; ++j) {
+        const int c = c0 + j;
+        const bool partial = c == chunks - 1 && last_cols < kChunkCols;
+        if (!partial) {
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+        }
+        uint32_t v[32];
+        epi_load_chunk<OUT>(tmem_acc, lane_field, c, v);
+        if (j == nc - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release();
+        }
+        if (partial)
+            epi_store_partial<OUT>(p, lane, m0, n0 + c * kChunkCols, last_cols, b, v);
+        else
+            epi_store_chunk<OUT>(p, tmC, slab, lane, m0, n0 + c * kChunkCols, b, v);
+    }
+}
+
 // Split-K epilogue of one warp (fp32 output; one tile per 2-CTA cluster, the
 // two CTAs holding the partial sums of the two halves of K).  The tile's
 // column chunks are shared out: CTA rank 0 owns chunks [0, h), rank 1 chunks

@@ -12,8 +12,14 @@
 //                        accumulating in tensor memory; tcgen05.commit frees
 //                        the group (split barrier) and, after the last K block,
 //                        publishes the accumulator.
-//   warps 2..5           epilogue: tcgen05.ld -> fp32/bf16/f16 -> conflict-free
-//                        swizzled st.shared -> TMA store (clips ragged edges).
+//   warps 2..5 (or 2..9) epilogue: tcgen05.ld -> fp32/bf16/f16 ->
+//                        conflict-free swizzled st.shared -> TMA store (clips
+//                        ragged edges).  A launch in which every CTA has one
+//                        tile (its epilogue is not overlapped by a next main
+//                        loop) of at most four column chunks has 8 epilogue
+//                        warps, two per tensor-memory lane quarter, each
+//                        taking half of the tile's chunks; with several tiles
+//                        per CTA 4 warps measured as fast or faster.
 // Two tensor-memory accumulators let the epilogue of tile i overlap the main
 // loop of tile i + 1.
 //
@@ -55,11 +61,15 @@ static_assert(kStageKBytes / kMmaKBytes == 4, "the issue loops unroll four MMAs 
 
 // KG: stages per full/empty barrier pair (1 or 2).  KIND: MmaKind.  SPLIT:
 // 1 = split-K over a 2-CTA cluster, one tile per cluster (fp32 output only).
-template <int OUT, int KG, int KIND, int SPLIT>
-__global__ void __launch_bounds__(kThreads, 1)
+// EPI8: 1 = eight epilogue warps (320 threads), for launches in which every
+// CTA has one tile of at most four column chunks.
+template <int OUT, int KG, int KIND, int SPLIT, int EPI8>
+__global__ void __launch_bounds__(EPI8 ? kWideThreads : kThreads, 1)
     smo_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const __grid_constant__ KParams p) {
     static_assert(!SPLIT || OUT == OUT_F32, "split-K partials meet in fp32");
+    static_assert(!(SPLIT && EPI8), "the split-K epilogue has four warps");
+    constexpr uint32_t epiw = EPI8 ? 8u : 4u;      // epilogue warps
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5;
@@ -89,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), kEpiWarps);
+            mbar_init(acce_bar(b), epiw);
         }
         mbar_init(drain_bar, 1);
         if (SPLIT) mbar_init(plain_bar, kEpiWarps * 32);
@@ -247,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(drain_bar, 0, budget)) report_error(p.err, DEV_TIMEOUT_TEARDOWN);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------ epilogue
+    } else if constexpr (SPLIT) {
+        // ------------------------------------------------ epilogue (split-K, warps 2..5)
         const uint32_t q = (uint32_t)warp & 3u;           // TMEM lane quarter of this warp
         const uint32_t lane_field = (q * 32u) << 16;
         uint32_t it = 0, sbuf = 0;
@@ -267,21 +277,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t m0 = mb * kBM + (int32_t)q * kEpiRowsPerWarp;
             const uint32_t slabs = base + p.off_epi + q * kEpiBufs * kEpiSlabBytes;
             const uint32_t acce = acce_bar(buf);
-            if constexpr (SPLIT) {
-                // one tile per cluster: the operand ring is idle once the
-                // accumulator is full; each warp stages the peer's chunks in
-                // its own 16 KiB of it
-                if (!epilogue_split_tile(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane,
-                                         m0, nb * p.BN, b, crank, base + q * 4u * kEpiSlabBytes,
-                                         mapa_shared(plain_bar, crank ^ 1u), plain_bar, budget,
-                                         [&] { mbar_arrive(acce); })) {
-                    if (lane == 0) report_error(p.err, DEV_TIMEOUT_SPLIT);
-                    break;
-                }
-            } else {
-                epilogue_tile<OUT>(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane, m0,
-                                   nb * p.BN, b, [&] { mbar_arrive(acce); });
+            // one tile per cluster: the operand ring is idle once the
+            // accumulator is full; each warp stages the peer's chunks in its
+            // own 16 KiB of it
+            if (!epilogue_split_tile(p, &tmC, tmem_base + buf * (uint32_t)p.BN, lane_field, slabs, sbuf, lane, m0,
+                                     nb * p.BN, b, crank, base + q * 4u * kEpiSlabBytes,
+                                     mapa_shared(plain_bar, crank ^ 1u), plain_bar, budget,
+                                     [&] { mbar_arrive(acce); })) {
+                if (lane == 0) report_error(p.err, DEV_TIMEOUT_SPLIT);
+                break;
             }
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5, or 2..9 with EPI8)
+        // warp 2 + e: tensor-memory lane quarter warp % 4 (the warps a CTA may
+        // read a quarter with); with 8 warps, chunk half e / 4 and one
+        // staging slab each, with 4 warps all chunks and two slabs each
+        const uint32_t e = (uint32_t)warp - 2u;
+        const uint32_t q = (uint32_t)warp & 3u;
+        const uint32_t lane_field = (q * 32u) << 16;
+        const int half = (p.epi_chunks + 1) / 2;
+        const int c0 = (int)(e >> 2) * half;
+        const int nc = min(p.epi_chunks - c0, half);
+        uint32_t it = 0, sbuf = 0;
+        for (int64_t t = tile0; t < p.total_tiles; t += tstride, ++it) {
+            int b, mb, nb;
+            decode_tile(p, t, b, mb, nb);
+            const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+            int good = 1;
+            if (lane == 0) good = mbar_wait(accf_bar(buf), aph, budget) ? 1 : 0;
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) {
+                if (lane == 0) report_error(p.err, DEV_TIMEOUT_EPILOGUE);
+                break;
+            }
+            tc_fence_after();
+            const int32_t m0 = mb * kBM + (int32_t)q * kEpiRowsPerWarp;
+            const uint32_t acce = acce_bar(buf);
+            const uint32_t acc = tmem_base + buf * (uint32_t)p.BN;
+            if constexpr (EPI8)
+                epilogue_tile_part<OUT>(p, &tmC, acc, lane_field, base + p.off_epi + e * kEpiSlabBytes, lane, m0,
+                                        nb * p.BN, b, c0, nc, p.epi_chunks, p.epi_last_cols,
+                                        [&] { mbar_arrive(acce); });
+            else
+                epilogue_tile<OUT>(p, &tmC, acc, lane_field, base + p.off_epi + q * kEpiBufs * kEpiSlabBytes, sbuf,
+                                   lane, m0, nb * p.BN, b, [&] { mbar_arrive(acce); });
         }
         if (lane == 0) bulk_wait<0>();
         __syncwarp();

@@ -11,8 +11,9 @@ constexpr int kStageKBytes = 128;   // K bytes per pipeline stage: one 128-byte 
 constexpr int kMmaKBytes = 32;      // K bytes per tcgen05.mma (kind::f16 K = 16, kind::f8f6f4 K = 32)
 constexpr int kThreads = 192;       // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
 constexpr int kEpiWarps = 4;
-// Wide CTA-pair tiles: 8 epilogue warps (two per tensor-memory lane quarter,
-// one per half of the tile's columns), 320 threads.
+// Wide CTA-pair tiles, and one-CTA launches with one tile per CTA: 8
+// epilogue warps (two per tensor-memory lane quarter, one per half of the
+// tile's columns), 320 threads.
 constexpr int kWideEpiWarps = 8;
 constexpr int kWideThreads = 64 + 32 * kWideEpiWarps;
 constexpr int kEpiRowsPerWarp = 32;

@@ -502,7 +502,7 @@ std::string describe_json(const Plan& p) {
       << ",\"tail_chunks\":" << p.tail_chunks << ",\"tail_last_cols\":" << p.tail_last_cols << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid
-      << ",\"group_m\":" << p.group_m << ",\"threads\":" << kThreads
+      << ",\"group_m\":" << p.group_m << ",\"threads\":" << (p.wide || (!p.pair && !p.split && p.tiles <= p.grid && p.c.chunks <= 4) ? kWideThreads : kThreads)
       << ",\"idesc\":" << p.idesc << ",\"smem_bytes\":" << p.smem_bytes
       << ",\"stage_stride\":" << p.stage_stride << ",\"off_epi\":" << p.off_epi
       << ",\"off_bar\":" << p.off_bar << ",\"tmem_cols\":" << p.tmem_cols;

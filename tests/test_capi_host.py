@@ -283,6 +283,30 @@ def test_tile_choice_and_grid(lib):
     assert d["pair"] and d["wide"] and d["BN"] == 256 and d["tiles"] == 4 * 8 * 32 and not d["tail"]
 
 
+def test_epilogue_warps_by_plan(lib, monkeypatch):
+    """Eight epilogue warps (320 threads) for wide pairs and for one-CTA
+    launches whose CTAs each hold one tile of at most four column chunks;
+    four (192 threads) otherwise."""
+    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f32")        # 108 tiles, 4 fp32 chunks
+    assert d["threads"] == 320 and d["tiles"] <= d["grid"] and d["C"]["chunks"] == 4
+    d = smo.gemm_plan_describe(256, 256, 256, 0, 1, "bf16", "bf16")        # 4 tiles, 2 bf16 chunks
+    assert d["threads"] == 320
+    d = smo.gemm_plan_describe(512, 512, 4096, 0, 1, "bf16", "f32")        # split K: four warps
+    assert d["split"] and d["threads"] == 192
+    d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")     # wide pair
+    assert d["wide"] and d["threads"] == 320
+    d = smo.gemm_plan_describe(16384, 8192, 1024, 0, 1, "bf16", "bf16")    # 256 x 256 pair
+    assert d["pair"] and not d["wide"] and d["threads"] == 192
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "256")
+    d = smo.gemm_plan_describe(2048, 2048, 1024, 0, 1, "bf16", "f32")      # one wave, 8 fp32 chunks
+    assert d["tiles"] <= d["grid"] and d["C"]["chunks"] == 8 and d["threads"] == 192
+    d = smo.gemm_plan_describe(2048, 2048, 1024, 0, 1, "bf16", "bf16")     # one wave, 4 bf16 chunks
+    assert d["threads"] == 320
+    monkeypatch.setenv("SMO_GEMM_FORCE_BN", "128")
+    d = smo.gemm_plan_describe(4096, 4096, 1024, 0, 1, "bf16", "bf16")     # several tiles per CTA
+    assert d["tiles"] > d["grid"] and d["threads"] == 192
+
+
 def test_split_k_policy(lib, monkeypatch):
     """Split-K is taken for fp32 output only, on one-CTA tiles; forced on it
     still keeps at least one K block per CTA; forced off the plan is the
