@@ -97,6 +97,9 @@ int gemm_bf16(const void* A, int64_t lda, int a_major,
  * out_dtype: GEMM_F32, GEMM_BF16 or GEMM_F16 (fp32 accumulator rounded to
  *            nearest-even on output).
  * batch >= 1 independent problems; strideA/B/C are ignored when batch == 1.
+ * Limits (else GEMM_ERR_UNSUPPORTED): M, N, K and batch below 2^31; lda, ldb
+ * and ldc below 2^32 elements; each batch stride below 2^40 bytes (the
+ * tensor-memory-access unit's stride limit).
  */
 int gemm_ex(const void* A, int64_t lda, int a_major,
             const void* B, int64_t ldb, int b_major,

@@ -508,12 +508,19 @@ int check_args(const void* A, int64_t lda, int a_major, const void* B, int64_t l
     if (M == 0 || N == 0) return 1;
     if (!C) return GEMM_ERR_ARG;
     const int64_t ies = elem_size(in_dtype), oes = elem_size(out_dtype);
+    // TMA strides stay below 2^40 bytes; these bounds also keep the extent
+    // arithmetic below within int64
+    constexpr int64_t kMaxLd = 1ll << 32, kMaxStrideBytes = 1ll << 40;
+    if (ldc >= kMaxLd || (batch > 1 && strideC >= kMaxStrideBytes / oes)) return GEMM_ERR_UNSUPPORTED;
     if (ldc < N) return GEMM_ERR_ARG;
     if (batch > 1 && strideC < (M - 1) * ldc + N) return GEMM_ERR_ARG;
     if ((reinterpret_cast<uintptr_t>(C) & 15) || (ldc * oes) % 16 || (batch > 1 && (strideC * oes) % 16))
         return GEMM_ERR_ALIGN;
     if (K == 0) return GEMM_OK;
     if (!A || !B) return GEMM_ERR_ARG;
+    if (lda >= kMaxLd || ldb >= kMaxLd ||
+        (batch > 1 && (strideA >= kMaxStrideBytes / ies || strideB >= kMaxStrideBytes / ies)))
+        return GEMM_ERR_UNSUPPORTED;
     const int64_t a_row = (a_major == GEMM_MN_MAJOR) ? M : K;
     const int64_t b_row = (b_major == GEMM_MN_MAJOR) ? N : K;
     if (lda < a_row || ldb < b_row) return GEMM_ERR_ARG;

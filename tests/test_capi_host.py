@@ -67,6 +67,11 @@ def test_argument_validation_without_device(lib):
     assert _ex(batch=2, sa=64 * 64, sb=64 * 64, sc=64) == smo.GEMM_ERR_ARG   # C batches overlap
     assert _ex(batch=2, sa=4100, sb=4096, sc=4096) == smo.GEMM_ERR_ALIGN
     assert _ex(M=1 << 31) == smo.GEMM_ERR_UNSUPPORTED
+    assert _ex(ldc=1 << 32) == smo.GEMM_ERR_UNSUPPORTED         # leading dimensions below 2^32
+    assert _ex(lda=1 << 32) == smo.GEMM_ERR_UNSUPPORTED
+    assert _ex(ldb=(1 << 32) + 64) == smo.GEMM_ERR_UNSUPPORTED
+    assert _ex(batch=2, sa=1 << 39, sb=4096, sc=4096) == smo.GEMM_ERR_UNSUPPORTED   # 2^40 bytes
+    assert _ex(batch=2, sa=4096, sb=4096, sc=1 << 38) == smo.GEMM_ERR_UNSUPPORTED   # fp32 C: 2^40 bytes
     assert _ex(i=5) == smo.GEMM_ERR_UNSUPPORTED        # no such input type
     # FP8 operands: one byte per element, so pitches need 16 elements
     assert _ex(i=3, lda=72, K=66) == smo.GEMM_ERR_ALIGN
@@ -74,6 +79,7 @@ def test_argument_validation_without_device(lib):
     # well-formed arguments reach the device query: no GPU here
     if not _have_gpu():
         assert _ex() == smo.GEMM_ERR_NO_DEVICE
+        assert _ex(K=0, lda=1 << 40) == smo.GEMM_ERR_NO_DEVICE   # K = 0: A and B unused
         assert _ex(i=3, lda=80, K=66) == smo.GEMM_ERR_NO_DEVICE
         assert smo.gemm_check(0) == smo.GEMM_ERR_NO_DEVICE
 
