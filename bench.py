@@ -339,18 +339,28 @@ def run_ours(args, world, rank, local):
                             "on every SM, no compute (smo_probe.h l2_read_probe)"}
         del pbuf, pout
 
-    for _ in range(args.warmup):
-        launch()
-    torch.cuda.synchronize(dev)
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     # Inputs + output larger than twice the 129 MB L2 stream from HBM anyway;
     # smaller working sets get L2 flushed (256 MiB written) before every launch,
     # and the flush's time is kept out of the step (see the timing below).
     work_bytes = (p.A.numel() + p.B.numel()) * p.A.element_size() + C.numel() * C.element_size()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if work_bytes < (258 << 20) else None
+
+    # The clock sampler starts first; the warm-up follows its start-up pause,
+    # so that the timed region begins on a busy GPU, not one that has idled.
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        launch()
+    if flush is not None and not args.graph:
+        # short launches timed one by one: keep the GPU busy for 50 ms first
+        # (after an idle pause its first microsecond-long launches run slow)
+        t_warm = time.perf_counter()
+        while time.perf_counter() - t_warm < 0.05:
+            flush.zero_()
+            launch()
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
     # per-launch event pairs only where flushes sit between host launches
     ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)] if flush is not None and not args.graph else [])

@@ -175,6 +175,10 @@ WORKLOADS: Dict[str, Dict] = {
     "batched_32x2048_bf16": dict(M=2048, N=2048, K=2048, batch=32, a_major=K_MAJOR,
                                  b_major=MN_MAJOR, in_dtype="bf16", out_dtype="bf16",
                                  dist="normal", sigma=0.02),
+    # a tile-starved long-K shape with fp32 output: 16 tiles of 128 x 128, K
+    # split over 2-CTA clusters
+    "gemm_512x512x4096_bf16_f32": dict(M=512, N=512, K=4096, a_major=K_MAJOR, b_major=MN_MAJOR,
+                                       in_dtype="bf16", out_dtype="f32", dist="uniform"),
     # 8-bit operands (E4M3), fp32 accumulate, bf16 out: the 8192^3 shape in the
     # transposed-B orientation and K-major B
     "gemm_8192_e4m3_bf16_AK_BN": dict(M=8192, N=8192, K=8192, a_major=K_MAJOR, b_major=MN_MAJOR,
