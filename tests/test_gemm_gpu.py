@@ -291,8 +291,9 @@ def test_config_256_bf16_f32():
 
 @pytest.mark.parametrize("split", ["auto", "0", "1"])
 def test_config_1500x1152x896_f16_uniform(split, monkeypatch):
-    """The planner splits K over 2-CTA clusters here (auto); forced off it runs
-    128 x 128 one-CTA tiles."""
+    """The planner keeps 108 one-CTA tiles of 128 x 128 here (auto: a split
+    is modelled, and measured, slower at K = 896); forced on, K is split over
+    2-CTA clusters."""
     if split != "auto":
         monkeypatch.setenv("SMO_GEMM_SPLIT_K", split)
     _full(workload("gemm_1500x1152x896_f16_f32"))
@@ -303,6 +304,15 @@ def test_config_1500x1152x896_f16_integer_bit_exact(split, monkeypatch):
     if split != "auto":
         monkeypatch.setenv("SMO_GEMM_SPLIT_K", split)
     _full(workload("gemm_1500x1152x896_f16_f32_int"), exact=True)
+
+
+def test_config_512x512x4096_split_k():
+    """The tile-starved long-K workload: the planner splits K over 2-CTA
+    clusters (16 tiles on 32 SMs)."""
+    p = workload("gemm_512x512x4096_bf16_f32")
+    assert smo.gemm_plan_describe(p.M, p.N, p.K, p.a_major, p.b_major, p.in_dtype, p.out_dtype)["split"]
+    _full(p)
+    _full(workload("gemm_512x512x4096_bf16_f32", dist="int"), exact=True)
 
 
 @pytest.mark.parametrize("name", ["gemm_4096_bf16_bf16_AK_BK", "gemm_4096_bf16_bf16_AK_BN",
