@@ -34,16 +34,26 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int64_t t, int& b,
 
 // Tile id -> (batch, m block, first column, width), with the tail region of a
 // wide tiling: tiles [tail_start, total_tiles) are tail_bn wide and cover M
-// blocks [tail_m0, tail_m0 + tail_gsz) x columns [tail_n0, N), in column
-// blocks of tail_gsz tiles.  Tiles before tail_start decode as decode_tile
-// does (the tail region is the end of the last M group's grouped order).
+// blocks [tail_m0, tail_m0 + tail_gsz) in column blocks of tail_gsz tiles --
+// the first tail_k0 of them columns [tail_n0, N) of problem tail_b0, then
+// tail_kfull per later problem, columns [0, N).  Tiles before tail_start
+// decode as decode_tile does (the tail region is the end of the grouped
+// order).
 __device__ __forceinline__ void decode_tile_w(const KParams& p, int64_t t, int& b, int& mb, int32_t& n0,
                                               int32_t& bn) {
     if (t >= p.tail_start) {
-        const int32_t r = (int32_t)(t - p.tail_start);
-        b = 0;
+        int32_t r = (int32_t)(t - p.tail_start);
+        int32_t base = p.tail_n0;
+        b = p.tail_b0;
+        if (r >= p.tail_k0) {
+            r -= p.tail_k0;
+            const int32_t j = r / p.tail_kfull;
+            b += 1 + j;
+            r -= j * p.tail_kfull;
+            base = 0;
+        }
         mb = p.tail_m0 + r % p.tail_gsz;
-        n0 = p.tail_n0 + (r / p.tail_gsz) * p.tail_bn;
+        n0 = base + (r / p.tail_gsz) * p.tail_bn;
         bn = p.tail_bn;
         return;
     }

@@ -94,6 +94,9 @@ struct KParams {
     int32_t serp;
     int64_t tail_start;
     int32_t tail_m0, tail_gsz, tail_n0, tail_bn;
+    // batches: tail tiles [0, tail_k0) lie in problem tail_b0 from column
+    // tail_n0; then tail_kfull tiles per later problem, from column 0
+    int32_t tail_b0, tail_k0, tail_kfull;
     uint32_t tail_idesc;
     int32_t tail_epi_chunks, tail_epi_last_cols;
     // Split-K over a 2-CTA cluster (one-CTA kernel, fp32 output): the CTA of

@@ -287,35 +287,47 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.num_n = (int)((N + bn - 1) / bn);
     p.tiles = tiles_for(p.tile_m, bn);
     p.group_m = std::min(p.pair ? 8 : 16, p.num_m);
-    // Tail of a wide tiling (256 wide, one problem): when the tiles leave a
-    // last wave only partly full and those tiles, in the grouped order, are
-    // the last q N blocks of the last M group, they are re-tiled with the
-    // narrowest width (a multiple of 16 that keeps the TMA coordinate rule)
-    // whose tiles still fit one wave: 8192^2 has 6 full waves of 76 tiles and
-    // 56 left over (8 M blocks x 7 N blocks); as 72 tiles of 512 x 208 the
-    // last wave takes 13/16 of a full one.
-    if (p.wide && bn == 256 && batch == 1 && force != 1024 && wide_bn == 0) {
+    // Tail of a wide tiling (256 wide): when the tiles leave a last wave only
+    // partly full and those tiles, in the grouped order, are whole columns of
+    // the last M group -- the last q N blocks of one problem, or, in a batch
+    // whose problems are one M group each, the last columns of one problem and
+    // the problems after it -- they are re-tiled with the narrowest width (a
+    // multiple of 16 that keeps the TMA coordinate rule) whose tiles still fit
+    // one wave: 8192^2 has 6 full waves of 76 tiles and 56 left over (8 M
+    // blocks x 7 N blocks); as 72 tiles of 512 x 208 the last wave takes
+    // 13/16 of a full one.  32 x 2048^2 leaves 36 tiles (the last column of
+    // one problem and the whole next one), re-tiled as 72 of 512 x 128.
+    const bool one_group = p.group_m == p.num_m;
+    if (p.wide && bn == 256 && (batch == 1 || one_group) && force != 1024 && wide_bn == 0) {
         const int64_t C = clusters;
         const int64_t T = p.tiles;
         const int64_t R = T % C;
-        const int gstart = ((p.num_m - 1) / p.group_m) * p.group_m;
+        const int gstart = batch == 1 ? ((p.num_m - 1) / p.group_m) * p.group_m : 0;
         const int gsz = p.num_m - gstart;
-        if (T / C >= 1 && R > 0 && R % gsz == 0 && R / gsz < p.num_n) {
-            const int q = (int)(R / gsz);
-            const int64_t n0 = (int64_t)(p.num_n - q) * bn;
-            const int64_t cols = N - n0;
-            const int64_t per_m = C / gsz;                    // tail N blocks that fit the wave
-            for (int w = 16; w < bn; w += 16) {
-                if (b_major && ((w / 2) * p.in_es) % 16 != 0) continue;
-                if ((cols + w - 1) / w > per_m) continue;
-                p.tail = 1;
-                p.tail_bn = w;
-                p.tail_m0 = gstart;
-                p.tail_gsz = gsz;
-                p.tail_n0 = (int)n0;
-                p.tail_start = T - R;
-                p.tail_tiles = (int)(gsz * ((cols + w - 1) / w));
-                break;
+        if (T / C >= 1 && R > 0 && R % gsz == 0) {
+            const int64_t q = R / gsz;                         // tail columns, in the grouped order
+            // problems after the first one the tail touches, and the first one's columns
+            const int64_t later = batch == 1 ? 0 : (q - 1) / p.num_n;
+            const int64_t q_first = q - later * p.num_n;
+            if (batch > 1 || q < p.num_n) {       // one problem: not its whole last group
+                const int64_t n0 = (int64_t)(p.num_n - q_first) * bn;
+                for (int w = 16; w < bn; w += 16) {
+                    if (b_major && ((w / 2) * p.in_es) % 16 != 0) continue;
+                    const int64_t k0 = gsz * ((N - n0 + w - 1) / w);
+                    const int64_t kfull = gsz * ((N + w - 1) / w);
+                    if (k0 + later * kfull > C) continue;
+                    p.tail = 1;
+                    p.tail_bn = w;
+                    p.tail_m0 = gstart;
+                    p.tail_gsz = gsz;
+                    p.tail_n0 = (int)n0;
+                    p.tail_b0 = (int)(batch - 1 - later);
+                    p.tail_k0 = (int)k0;
+                    p.tail_kfull = (int)kfull;
+                    p.tail_start = T - R;
+                    p.tail_tiles = (int)(k0 + later * kfull);
+                    break;
+                }
             }
         }
         if (p.tail) p.tiles = p.tail_start + p.tail_tiles;
@@ -471,6 +483,9 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->tail_gsz = p.tail_gsz;
     kp->tail_n0 = p.tail_n0;
     kp->tail_bn = p.tail_bn;
+    kp->tail_b0 = p.tail_b0;
+    kp->tail_k0 = p.tail_tiles == 0 ? 0 : p.tail_k0;
+    kp->tail_kfull = p.tail_kfull > 0 ? p.tail_kfull : 1;
     kp->tail_idesc = p.tail_idesc;
     kp->tail_epi_chunks = p.tail_chunks;
     kp->tail_epi_last_cols = p.tail_last_cols;
@@ -498,7 +513,8 @@ std::string describe_json(const Plan& p) {
       << ",\"pair\":" << p.pair << ",\"wide\":" << p.wide << ",\"split\":" << p.split
       << ",\"split_kh\":" << p.split_kh << ",\"tail\":" << p.tail << ",\"tail_start\":" << p.tail_start
       << ",\"tail_m0\":" << p.tail_m0 << ",\"tail_gsz\":" << p.tail_gsz << ",\"tail_n0\":" << p.tail_n0
-      << ",\"tail_bn\":" << p.tail_bn << ",\"tail_tiles\":" << p.tail_tiles << ",\"tail_idesc\":" << p.tail_idesc
+      << ",\"tail_bn\":" << p.tail_bn << ",\"tail_tiles\":" << p.tail_tiles << ",\"tail_b0\":" << p.tail_b0
+      << ",\"tail_k0\":" << p.tail_k0 << ",\"tail_kfull\":" << p.tail_kfull << ",\"tail_idesc\":" << p.tail_idesc
       << ",\"tail_chunks\":" << p.tail_chunks << ",\"tail_last_cols\":" << p.tail_last_cols << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid

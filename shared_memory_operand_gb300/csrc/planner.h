@@ -59,6 +59,9 @@ struct Plan {
     int tail = 0;
     int64_t tail_start = 0;
     int tail_m0 = 0, tail_gsz = 0, tail_n0 = 0, tail_bn = 0, tail_tiles = 0;
+    // batches: the tail starts in problem tail_b0 at column tail_n0 (its first
+    // tail_k0 tiles); each later problem is re-tiled whole (tail_kfull tiles)
+    int tail_b0 = 0, tail_k0 = 0, tail_kfull = 0;
     uint32_t tail_idesc = 0;
     int tail_chunks = 0, tail_last_cols = 0;
     int split_kh = 0;               // K blocks of the cluster's rank-0 CTA

@@ -286,7 +286,8 @@ def test_tile_choice_and_grid(lib):
     assert d["grid"] == 152 and d["stages"] == 6 and d["A"]["tile_mn"] == d["B"]["tile_mn"] == 128
     # 32 K blocks: wide 512 x 256 tiles (measured +1.8% over 256 x 256 here)
     d = smo.gemm_plan_describe(2048, 2048, 2048, 0, 1, "bf16", "bf16", batch=32)
-    assert d["pair"] and d["wide"] and d["BN"] == 256 and d["tiles"] == 4 * 8 * 32 and not d["tail"]
+    assert d["pair"] and d["wide"] and d["BN"] == 256 and d["tail_start"] == 13 * 76
+    assert d["tail"] and d["tail_bn"] == 128 and d["tiles"] == 13 * 76 + 72      # the last wave re-tiled
 
 
 def test_epilogue_warps_by_plan(lib, monkeypatch):
@@ -392,27 +393,43 @@ def test_tma_coordinate_rule_refuses_unaligned_widths(lib, monkeypatch):
 
 
 def _tiles_of(d):
-    """The output rectangles of a plan's tiles, decoded as the wide CTA-pair
-    kernel decodes them: tiles before tail_start in groups of group_m M blocks,
-    column-major inside a group; the tail region in column blocks of tail_gsz
-    tiles, tail_bn wide."""
+    """The output rectangles (batch entry, first row, first column, width) of
+    a plan's tiles, decoded as the wide CTA-pair kernel decodes them: tiles
+    before tail_start problem by problem, in groups of group_m M blocks,
+    column-major inside a group; the tail region in column blocks of
+    tail_gsz tiles, tail_bn wide -- tail_k0 tiles of problem tail_b0 from
+    column tail_n0, then tail_kfull per later problem from column 0."""
     BM, BN, gm = d["BM"], d["BN"], d["group_m"]
     num_m, num_n = d["num_m"], d["num_n"]
+    per_batch = num_m * num_n
     out = []
     for t in range(d["tiles"]):
         if d["tail"] and t >= d["tail_start"]:
             r = t - d["tail_start"]
+            b, base = d["tail_b0"], d["tail_n0"]
+            if r >= d["tail_k0"]:
+                r -= d["tail_k0"]
+                j = r // d["tail_kfull"]
+                b, r, base = b + 1 + j, r - j * d["tail_kfull"], 0
             mb = d["tail_m0"] + r % d["tail_gsz"]
-            n0 = d["tail_n0"] + (r // d["tail_gsz"]) * d["tail_bn"]
-            out.append((mb * BM, n0, d["tail_bn"]))
+            out.append((b, mb * BM, base + (r // d["tail_gsz"]) * d["tail_bn"], d["tail_bn"]))
             continue
+        b, r = divmod(t, per_batch)
         span = gm * num_n
-        g = t // span
+        g = r // span
         first = g * gm
         gsz = min(num_m - first, gm)
-        rr = t - g * span
-        out.append(((first + rr % gsz) * BM, (rr // gsz) * BN, BN))
+        rr = r - g * span
+        out.append((b, (first + rr % gsz) * BM, (rr // gsz) * BN, BN))
     return out
+
+
+def _assert_covers_once(d, M, N, batch=1):
+    cover = np.zeros((batch, -(-M // 512) * 512, N + 256), dtype=np.int8)
+    for (b, m0, n0, w) in _tiles_of(d):
+        assert 0 <= b < batch
+        cover[b, m0:m0 + 512, n0:n0 + w] += 1
+    assert np.all(cover[:, :M, :N] == 1)
 
 
 @pytest.mark.parametrize("M,N,K,bm,ind", [(8192, 8192, 8192, 1, "bf16"), (8192, 8192, 8192, 0, "bf16"),
@@ -431,10 +448,32 @@ def test_wide_tail_covers_the_output_once(lib, M, N, K, bm, ind):
         assert (d["tail_bn"] // 2 * es) % 16 == 0 and (d["tail_n0"] * es) % 16 == 0
     x = d["tail_idesc"]
     assert ((x >> 17) & 63) * 8 == d["tail_bn"] and ((x >> 24) & 31) * 16 == 256
-    cover = np.zeros((-(-M // 512) * 512, N + 256), dtype=np.int8)
-    for (m0, n0, w) in _tiles_of(d):
-        cover[m0:m0 + 512, n0:n0 + w] += 1
-    assert np.all(cover[:M, :N] == 1)
+    _assert_covers_once(d, M, N)
+
+
+@pytest.mark.parametrize("M,N,batch,bm,later", [
+    (2048, 2048, 32, 1, 1),      # the batched workload: last column of entry 30, all of entry 31
+    (2048, 2048, 32, 0, 1),
+    (1024, 2048, 31, 1, 2),      # the tail spans three entries
+    (2048, 1280, 21, 1, 1),      # the first entry the tail touches is re-tiled whole
+    (1500, 2048, 12, 1, 2),      # ragged M (three M blocks, the last one 476 rows)
+    (2560, 2048, 20, 1, 0),      # five M blocks
+    (1024, 4096, 31, 1, 0),      # 16-wide tail tiles
+])
+def test_batched_wide_tail_covers_every_entry_once(lib, M, N, batch, bm, later):
+    """A batch of problems that are one M group each: the tiles left for a
+    last, partial wave are whole columns at the end of the order, from the
+    last columns of one problem and all of the problems after it; re-tiled
+    narrower, they fit one wave and every output element of every problem
+    is covered exactly once."""
+    d = smo.gemm_plan_describe(M, N, 2048, 0, bm, "bf16", "bf16", batch, 152)
+    assert d["ok"] and d["wide"] and d["tail"], d
+    assert d["group_m"] == d["num_m"] and d["tail_start"] % 76 == 0 and d["tail_tiles"] <= 76
+    assert (d["tail_tiles"] - d["tail_k0"]) // d["tail_kfull"] == later
+    assert d["tail_b0"] == batch - 1 - later and d["tail_bn"] < 256
+    if bm:
+        assert (d["tail_bn"] // 2 * 2) % 16 == 0
+    _assert_covers_once(d, M, N, batch)
 
 
 def test_wide_tail_off_when_forced_or_full(lib, monkeypatch):

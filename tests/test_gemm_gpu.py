@@ -528,3 +528,20 @@ def test_wide_tail_full_compare(M, N, K, bm, ind, out, dist):
     assert plan["tail"] == 1
     p = make_problem(M, N, K, a_major=K_MAJOR, b_major=bm, in_dtype=ind, out_dtype=out, dist=dist, seed=M + N)
     _full(p, exact=(dist == "int"))
+
+
+@pytest.mark.parametrize("M,N,batch,bm,out,dist,b0", [
+    (1024, 2048, 31, MN_MAJOR, "bf16", "uniform", 28),   # the tail spans three entries
+    (2048, 1280, 21, K_MAJOR, "f32", "int", 19),          # the first entry it touches re-tiled whole, exact
+    (1500, 2048, 12, MN_MAJOR, "bf16", "normal", 9),      # ragged M (three M blocks, the last one 476 rows)
+    (1024, 4096, 31, MN_MAJOR, "f32", "int", 30),         # 16-wide tail tiles in the last entry, exact
+])
+def test_batched_wide_tail_full_compare(M, N, batch, bm, out, dist, b0):
+    """A batch whose last, partial wave is re-tiled narrower, within the last
+    entry or across entries (tail tiles decode to their own entry, rows and
+    columns)."""
+    plan = smo.gemm_plan_describe(M, N, 2048, K_MAJOR, bm, "bf16", out, batch)
+    assert plan["wide"] and plan["tail"] and plan["tail_b0"] == b0
+    p = make_problem(M, N, 2048, a_major=K_MAJOR, b_major=bm, out_dtype=out, dist=dist, batch=batch,
+                     seed=M + N + batch)
+    _full(p, exact=(dist == "int"))
