@@ -146,3 +146,16 @@ def test_split_k_fp8(am, bm, monkeypatch):
                          seed=M + K)
         assert smo.gemm_plan_describe(M, N, K, am, bm, "e4m3", "f32")["split"] == 1
         _full(p, exact=(dist == "int"))
+
+
+@pytest.mark.parametrize("bm,tail_bn", [(K_MAJOR, 176), (MN_MAJOR, 192)])
+@pytest.mark.parametrize("out,dist", [("bf16", "uniform"), ("f32", "int")])
+def test_batched_wide_tail_fp8(bm, tail_bn, out, dist):
+    """FP8 operands in a batch whose last wave is re-tiled narrower across
+    batch entries (an N-major FP8 B half-tile starts on a 16-byte boundary, so
+    its tail width is a multiple of 32); integers bit-exact."""
+    plan = smo.gemm_plan_describe(512, 1024, 4096, K_MAJOR, bm, "e4m3", out, 31)
+    assert plan["wide"] and plan["tail"] and plan["tail_bn"] == tail_bn and plan["tail_b0"] == 19
+    p = make_problem(512, 1024, 4096, a_major=K_MAJOR, b_major=bm, in_dtype="e4m3", out_dtype=out,
+                     dist=dist, batch=31, seed=bm + 7)
+    _full(p, exact=(dist == "int"))
