@@ -596,6 +596,8 @@ int run_gemm(DevState& ds, int32_t* err, int stream_k, const void* A, int64_t ld
     kp.kgroup = kgroup_from_env(kp.kgroup, kp.stages, pl->pair);
     kp.serp = pl->wide ? serpentine_from_env() : 0;
     kp.group_m = group_m_from_env(kp.group_m, kp.num_m);
+    if (const char* e = std::getenv("SMO_GEMM_EPI_PACE"))   // measurement knob: 0 = stores back to back
+        if (e[0] == '0') kp.epi_pace_ns_per_kb = 0;
 
     switch (out_dtype) {
         case GEMM_F32: return launch<smo::OUT_F32>(*pl, ds, ta, tb, tc, kp, stream, stream_k);

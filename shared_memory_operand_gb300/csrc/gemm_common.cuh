@@ -513,6 +513,40 @@ __device__ __forceinline__ void epilogue_tile(const KParams& p, const CUtensorMa
                        p.epi_last_cols);
 }
 
+// Epilogue of one warp of a 256 x 256 CTA-pair tile with 16-bit output (four
+// whole 64-column chunks): the warp reads all four chunks into registers
+// (128 per thread, packed), hands the accumulator back -- the MMA issuer
+// starts the tile after next at once -- and then stores chunk j no earlier
+// than j x pace_ns after the hand-back, so that the tile's C leaves the SM
+// spread over the next tile's main loop instead of in one burst against its
+// operand loads (pace_ns = 0: back to back).  The waits are bounded by
+// 3 x pace_ns.
+template <int OUT, typename Release>
+__device__ __forceinline__ void epilogue_tile_paced(const KParams& p, const CUtensorMap* tmC, uint32_t acc,
+                                                    uint32_t lane_field, uint32_t slabs, uint32_t& sbuf, int lane,
+                                                    int32_t m0, int32_t n0, int b, int64_t pace_ns,
+                                                    Release release) {
+    static_assert(OUT != OUT_F32, "16-bit output");
+    uint32_t v[4][32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) epi_load_chunk_halves<OUT>(acc, lane_field, j, v[j]);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release();
+    const uint64_t t0 = globaltimer();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j > 0 && pace_ns > 0 && lane == 0) {
+            const uint64_t until = t0 + (uint64_t)j * (uint64_t)pace_ns;
+            while (globaltimer() < until) __nanosleep(128);
+        }
+        if (lane == 0) bulk_wait_read<1>();         // the slab's previous store has read it
+        __syncwarp();
+        epi_store_chunk<OUT>(p, tmC, slabs + sbuf * kEpiSlabBytes, lane, m0, n0 + j * 64, b, v[j]);
+        sbuf ^= 1u;
+    }
+}
+
 // One of eight epilogue warps of a one-CTA tile: tensor-memory lane quarter
 // `lane_field`, chunks [c0, c0 + nc) of the tile's `chunks` (the last one
 // holding `last_cols` columns), staged through the warp's one slab.  With at

@@ -394,6 +394,18 @@ __global__ void __launch_bounds__(WIDE ? kWideThreads : kThreads, 1)
                     if (lane == 0) report_error(p.err, DEV_TIMEOUT_FIXUP);
                 }
             }
+            if constexpr (WIDE == 0 && OUT != OUT_F32) {
+                if (p.epi_pace_ns_per_kb > 0 && w.role == ROLE_WHOLE && chunks == 4 && last_cols == 64) {
+                    const int32_t m0 = mb * (2 * kBM) + (int32_t)rank * kBM + (int32_t)q * kEpiRowsPerWarp;
+                    // spaced only while this cluster has a next main loop to
+                    // hide the stores behind (the last tile stores at once)
+                    const bool more = wi.dp < p.dp_tiles || wi.u < wi.u1;
+                    epilogue_tile_paced<OUT>(p, &tmC, acc, lane_field, slabs, sbuf, lane, m0, n0, b,
+                                             more ? (int64_t)p.epi_pace_ns_per_kb * (w.kb1 - w.kb0) : 0,
+                                             [&] { mbar_arrive_cluster(acce); });
+                    continue;
+                }
+            }
             for (int i = 0; i < MSUB; ++i) {
                 // CTA `rank`'s accumulator region i holds tile rows rank * 128 * MSUB + i * 128 ...
                 const int32_t m0 = mb * (2 * MSUB * kBM) + (int32_t)rank * (MSUB * kBM) + i * kBM +

@@ -72,6 +72,9 @@ struct KParams {
     int32_t epi_chunk_cols;         // output columns per 128-byte chunk
     int32_t epi_chunks;             // chunks per tile row (ceil(BN / epi_chunk_cols))
     int32_t epi_last_cols;          // tile columns in the last chunk (epi_chunk_cols unless BN is not a multiple)
+    // 256 x 256 pair tiles with 16-bit output: spacing of a warp's four chunk
+    // stores, in ns per K block of the tile (0: stored back to back)
+    int32_t epi_pace_ns_per_kb;
     void* C;                        // output base (ragged 16-byte row tails are stored directly)
     int64_t ldc, strideC;           // elements
     int32_t n_tma;                  // columns [0, n_tma) are written by TMA (n_tma * es % 16 == 0)

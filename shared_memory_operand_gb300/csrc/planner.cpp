@@ -374,6 +374,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int a_major, int b_major, int in
     p.c.chunk_cols = 128 / p.c.out_es;
     p.c.chunks = (bn + p.c.chunk_cols - 1) / p.c.chunk_cols;
     p.c.last_cols = bn - (p.c.chunks - 1) * p.c.chunk_cols;
+    // 256 x 256 pair tiles with 16-bit output: each epilogue warp reads its
+    // four chunks into registers, hands the accumulator back and spaces the
+    // four stores over about half of the next tile's main loop instead of
+    // issuing them in one burst, which competed with that loop's operand
+    // loads for the SM's path to L2 (measured on 16384 x 8192 x 1024: +1.5%
+    // for the early hand-back, +2.9% with 40-56 ns per K block, -9% at 85,
+    // where the stores run into the next epilogue).  A K block takes about
+    // 265 ns at the 16-bit MMA rate and half that with FP8.
+    if (p.pair && !p.wide && out_dtype != 2 && p.c.chunks == 4 && p.c.last_cols == p.c.chunk_cols)
+        p.epi_pace_ns_per_kb = p.in_es == 1 ? 24 : 48;
     if (p.tail) {
         p.tail_chunks = (p.tail_bn + p.c.chunk_cols - 1) / p.c.chunk_cols;
         p.tail_last_cols = p.tail_bn - (p.tail_chunks - 1) * p.c.chunk_cols;
@@ -483,6 +493,7 @@ void fill_params(const Plan& p, KParams* kp) {
     kp->tail_gsz = p.tail_gsz;
     kp->tail_n0 = p.tail_n0;
     kp->tail_bn = p.tail_bn;
+    kp->epi_pace_ns_per_kb = p.epi_pace_ns_per_kb;
     kp->tail_b0 = p.tail_b0;
     kp->tail_k0 = p.tail_tiles == 0 ? 0 : p.tail_k0;
     kp->tail_kfull = p.tail_kfull > 0 ? p.tail_kfull : 1;
@@ -514,7 +525,8 @@ std::string describe_json(const Plan& p) {
       << ",\"split_kh\":" << p.split_kh << ",\"tail\":" << p.tail << ",\"tail_start\":" << p.tail_start
       << ",\"tail_m0\":" << p.tail_m0 << ",\"tail_gsz\":" << p.tail_gsz << ",\"tail_n0\":" << p.tail_n0
       << ",\"tail_bn\":" << p.tail_bn << ",\"tail_tiles\":" << p.tail_tiles << ",\"tail_b0\":" << p.tail_b0
-      << ",\"tail_k0\":" << p.tail_k0 << ",\"tail_kfull\":" << p.tail_kfull << ",\"tail_idesc\":" << p.tail_idesc
+      << ",\"tail_k0\":" << p.tail_k0 << ",\"tail_kfull\":" << p.tail_kfull
+      << ",\"epi_pace_ns_per_kb\":" << p.epi_pace_ns_per_kb << ",\"tail_idesc\":" << p.tail_idesc
       << ",\"tail_chunks\":" << p.tail_chunks << ",\"tail_last_cols\":" << p.tail_last_cols << ",\"BM\":" << p.tile_m << ",\"BN\":" << p.BN << ",\"BK\":" << p.bk << ",\"mma_k\":" << p.mma_k << ",\"kind\":" << p.kind << ",\"in_es\":" << p.in_es
       << ",\"stages\":" << p.stages << ",\"kgroup\":" << p.kgroup << ",\"num_m\":" << p.num_m << ",\"num_n\":" << p.num_n
       << ",\"num_k\":" << p.num_k << ",\"tiles\":" << p.tiles << ",\"grid\":" << p.grid

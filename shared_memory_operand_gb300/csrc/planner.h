@@ -62,6 +62,9 @@ struct Plan {
     // batches: the tail starts in problem tail_b0 at column tail_n0 (its first
     // tail_k0 tiles); each later problem is re-tiled whole (tail_kfull tiles)
     int tail_b0 = 0, tail_k0 = 0, tail_kfull = 0;
+    // 256 x 256 pair tiles, 16-bit output (four whole chunks per warp): the
+    // epilogue spaces its chunk stores by this many ns per K block of a tile
+    int epi_pace_ns_per_kb = 0;
     uint32_t tail_idesc = 0;
     int tail_chunks = 0, tail_last_cols = 0;
     int split_kh = 0;               // K blocks of the cluster's rank-0 CTA

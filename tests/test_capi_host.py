@@ -314,6 +314,22 @@ def test_epilogue_warps_by_plan(lib, monkeypatch):
     assert d["tiles"] > d["grid"] and d["threads"] == 192
 
 
+def test_epilogue_pacing_by_plan(lib):
+    """256 x 256 pair tiles with 16-bit output space their chunk stores (48 ns
+    per K block for 16-bit operands, 24 for FP8, whose K blocks take half the
+    time); fp32 output, wide and one-CTA tiles store back to back."""
+    d = smo.gemm_plan_describe(16384, 8192, 1024, 0, 1, "bf16", "bf16")
+    assert d["pair"] and not d["wide"] and d["epi_pace_ns_per_kb"] == 48
+    d = smo.gemm_plan_describe(16384, 8192, 2048, 0, 1, "e4m3", "bf16")
+    assert d["pair"] and not d["wide"] and d["epi_pace_ns_per_kb"] == 24
+    d = smo.gemm_plan_describe(16384, 8192, 1024, 0, 1, "bf16", "f32")
+    assert d["pair"] and not d["wide"] and d["epi_pace_ns_per_kb"] == 0
+    d = smo.gemm_plan_describe(8192, 8192, 8192, 0, 1, "bf16", "bf16")
+    assert d["wide"] and d["epi_pace_ns_per_kb"] == 0
+    d = smo.gemm_plan_describe(1500, 1152, 896, 0, 1, "f16", "f16")
+    assert not d["pair"] and d["epi_pace_ns_per_kb"] == 0
+
+
 def test_split_k_policy(lib, monkeypatch):
     """Split-K is taken for fp32 output only, on one-CTA tiles; forced on it
     still keeps at least one K block per CTA; forced off the plan is the

@@ -348,6 +348,23 @@ def test_config_skinny():
     _full(workload("skinny_16384x8192x1024_bf16"))
 
 
+@pytest.mark.parametrize("ind,out", [("bf16", "bf16"), ("f16", "f16"), ("e4m3", "bf16")])
+def test_paced_epilogue_matches_back_to_back(ind, out, monkeypatch):
+    """256 x 256 pair tiles with 16-bit output: the epilogue that reads the
+    whole accumulator and spaces its stores gives the same bits as the one
+    that stores chunk by chunk, and matches the oracle; several tiles per
+    cluster, ragged edges."""
+    p = make_problem(3000, 2900, 1024, a_major=K_MAJOR, b_major=MN_MAJOR, in_dtype=ind, out_dtype=out,
+                     dist="uniform", seed=17)
+    plan = smo.gemm_plan_describe(p.M, p.N, p.K, p.a_major, p.b_major, ind, out)
+    assert plan["pair"] and not plan["wide"] and plan["epi_pace_ns_per_kb"] > 0 and plan["tiles"] > 76
+    paced = run_gpu(p)
+    monkeypatch.setenv("SMO_GEMM_EPI_PACE", "0")
+    plain = run_gpu(p)
+    assert np.array_equal(paced, plain)
+    check(p, paced, oracle_full(p))
+
+
 def test_config_batched():
     _full(workload("batched_32x2048_bf16"))
 
