@@ -511,3 +511,31 @@ def test_pair_descriptors(lib, monkeypatch):
             assert ((x >> 24) & 31) * 16 == 256 and ((x >> 17) & 63) * 8 == 256
             assert d["stage_stride"] == 2 * 128 * 64 * 2
             assert d["tmem_cols"] == 512
+
+
+def test_wide_tail_random_shapes_cover_once(lib):
+    """Seeded random shapes, batches, orientations and operand types: whenever
+    the planner re-tiles a wide tiling's last wave, every output element of
+    every batch entry is covered exactly once, the tail fits one wave of 76
+    clusters and keeps the TMA coordinate rule."""
+    rng = np.random.default_rng(12345)
+    seen = 0
+    for _ in range(1500):
+        batch = int(rng.choice([1, 1, 1, 2, 3, 5, 8, 12, 17, 31, 32, 40]))
+        M = int(rng.integers(256, 12000 if batch == 1 else 3000))
+        N = int(rng.integers(256, 12000 if batch == 1 else 3000)) // 16 * 16 + 16
+        if batch * M * N > 60_000_000:
+            continue
+        ind = str(rng.choice(["bf16", "f16", "e4m3"]))
+        bm = int(rng.integers(0, 2))
+        K = 8192 if ind == "e4m3" else 4096
+        d = smo.gemm_plan_describe(M, N, K, 0, bm, ind, "bf16", batch, 152)
+        if not (d["ok"] and d["wide"] and d["tail"]):
+            continue
+        seen += 1
+        es = 1 if ind == "e4m3" else 2
+        assert d["tail_start"] % 76 == 0 and 0 < d["tail_tiles"] <= 76 and 16 <= d["tail_bn"] < 256
+        if bm:
+            assert (d["tail_bn"] // 2 * es) % 16 == 0 and (d["tail_n0"] * es) % 16 == 0
+        _assert_covers_once(d, M, N, batch)
+    assert seen >= 30
